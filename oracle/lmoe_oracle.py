@@ -1,0 +1,273 @@
+"""fp64 CPU oracle of the Stable LatentMoE layer forward.
+
+TEST INFRASTRUCTURE.  Only the test-suite, the smoke check and the benchmark's
+CPU-baseline / reference legs may import or run this module.  The CUDA library
+never calls it and shares no code with it; both receive the same seeded inputs
+from the separate input-generator module.
+
+Everything is computed in float64 with numpy; bf16 / fp32 inputs are upcast
+exactly.  Intermediates are never rounded to a narrower type.  The code follows
+the layer as the pages state it, with every silent point taken as listed below.
+
+Sources (cited by page title and section):
+  [K3-news] "KimiK3的StableLatentMoE架构解析, 轻量化大模型如何解决专家负载失衡与数值失稳"
+            (tech.news18a.com/article/17525): the module list (¶"从代码结构看", Fig. 1),
+            the forward order (¶"具体前向流程", Fig. 2), SiTU-GLU (¶"第一"),
+            RMSNorm before up (¶"第二"), Quantile Balancing with sigmoid gating (¶"第三").
+  [K3-arch] "Vue d'ensemble de l'architecture" (mkdocs.reaper.mx, kimi-k3/architecture/
+            01-vue-d-ensemble): "Le budget de paramètres, module par module" (table) and
+            "Par où l'information passe, pour un seul jeton" (steps c-g).
+
+Readings of the silent points (the same list is kept with the design notes):
+  A1  act(g, u) = g' * sigmoid(g') * u',  g' = beta*tanh(g/beta), u' = beta_u*tanh(u/beta_u),
+      beta = 4, beta_u = 25 ([K3-news] ¶"第一" names only "sigmoid limiting + tanh scaling
+      with an upper bound").
+  A2  the same beta / beta_u in routed and shared experts.
+  A3  the router reads x at width d (its 896 x 7168 = 6.4 M parameters, [K3-arch] table).
+  A4  scores s = sigmoid(logit), no temperature.  An optional per-expert additive logit
+      bias (used only by the skewed workload) is part of the logits.
+  A5  alpha_e = linear-interpolation (type 7) quantile at q = 1 - K/E of s[:, e] over the
+      tokens of one call; no state across calls.
+  A6  exactly K experts per token: the K largest keys s - alpha; no capacity, no drops.
+  A7  ties go to the lower expert index; idx is ordered by key, descending.
+  A8  combine weight w = s / (sum of s over the chosen K); raw scores, not s - alpha.
+  A9  RMSNorm is applied to each (token, expert) latent output, before the weighted sum.
+  A10 eps = 1e-6, learnable gain gamma in R^latent.
+  A11 W_up is applied once, to the weighted latent sum.
+  A12 layer output = routed + shared (the block residual is outside the layer).
+  A13 expert and shared intermediate size 3072 (derived from 33.0 M and 66 M).
+
+parity unpinned: whether A1, A5, A8 and A9 match the real Kimi K3 layer.  The pages
+cannot decide that; the pins in the test-suite fix this oracle to the readings above.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# --------------------------------------------------------------------------- shapes
+
+def param_counts(d: int, latent: int, n_experts: int, top_k: int, expert_inter: int,
+                 n_shared: int, shared_inter: int) -> dict:
+    """Parameter counts per module of one layer ([K3-arch] "Le budget de paramètres,
+    module par module"; "Par où l'information passe", steps c-g)."""
+    per_expert = 3 * latent * expert_inter          # gate, up: [I, L]; down: [L, I]
+    per_shared = 3 * d * shared_inter
+    return {
+        "router": n_experts * d,
+        "w_down": latent * d,
+        "w_up": d * latent,
+        "per_expert": per_expert,
+        "experts_total": n_experts * per_expert,
+        "experts_active": top_k * per_expert,
+        "per_shared": per_shared,
+        "shared_total": n_shared * per_shared,
+    }
+
+
+# --------------------------------------------------------------------------- routing
+
+def sigmoid(v: np.ndarray) -> np.ndarray:
+    """Logistic function; the router's score ([K3-news] ¶"第三": sigmoid gating)."""
+    v = np.asarray(v, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-v))
+
+
+def router_logits(x: np.ndarray, w_router: np.ndarray, bias: np.ndarray | None = None) -> np.ndarray:
+    """l[t, e] = sum_i x[t, i] * W_r[e, i] (+ b_e): the router scores every token against
+    every expert at model width ([K3-arch] step c: 896 scores, 6.4 M parameters)."""
+    l = np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
+    if bias is not None:
+        l = l + np.asarray(bias, np.float64)[None, :]
+    return l
+
+
+def quantile_position(bt: int, n_experts: int, top_k: int) -> tuple[int, float]:
+    """Position of the q = 1 - K/E quantile among bt sorted values, type 7:
+    h = (bt - 1) * q = (bt - 1) * (E - K) / E, split exactly into j = floor(h) and h - j."""
+    num = (bt - 1) * (n_experts - top_k)
+    j = num // n_experts
+    frac = (num - j * n_experts) / n_experts
+    return j, frac
+
+
+def quantile_cutoff(s: np.ndarray, top_k: int) -> np.ndarray:
+    """Per-expert Quantile Balancing cutoff alpha_e ([K3-news] ¶"第三": a threshold per
+    expert that steers its token count toward the quantile target; reading A5).
+
+    alpha_e = v_j + (h - j) * (v_{j+1} - v_j) with v the ascending sort of s[:, e]."""
+    s = np.asarray(s, np.float64)
+    bt, n_experts = s.shape
+    j, frac = quantile_position(bt, n_experts, top_k)
+    v = np.sort(s, axis=0)
+    vj = v[j]
+    if j + 1 >= bt:
+        return vj.copy()
+    return vj + frac * (v[j + 1] - vj)
+
+
+def topk_select(s: np.ndarray, alpha: np.ndarray, top_k: int) -> tuple[np.ndarray, np.ndarray]:
+    """Per token, the K experts with the largest key s - alpha (A6), ties to the lower
+    expert index, listed by key descending (A7) ([K3-news] ¶"具体前向流程": top-16).
+
+    Returns (idx [bt, K] int32, sorted_keys [bt, E] float64 in selection order)."""
+    keys = np.asarray(s, np.float64) - np.asarray(alpha, np.float64)[None, :]
+    bt, n_experts = keys.shape
+    eidx = np.broadcast_to(np.arange(n_experts), keys.shape)
+    order = np.lexsort((eidx, -keys), axis=-1)        # primary: key desc; secondary: e asc
+    idx = order[:, :top_k].astype(np.int32)
+    sorted_keys = np.take_along_axis(keys, order, axis=-1)
+    return idx, sorted_keys
+
+
+def combine_weights(s: np.ndarray, idx: np.ndarray) -> np.ndarray:
+    """w[t, k] = s[t, idx[t, k]] / sum_k' s[t, idx[t, k']] (reading A8 of the "weighted
+    fusion" in [K3-news] ¶"具体前向流程"); the sum runs in k order."""
+    s = np.asarray(s, np.float64)
+    chosen = np.take_along_axis(s, idx.astype(np.int64), axis=1)
+    total = np.zeros(chosen.shape[0])
+    for k in range(chosen.shape[1]):
+        total = total + chosen[:, k]
+    return chosen / total[:, None]
+
+
+def expert_counts(idx: np.ndarray, n_experts: int) -> np.ndarray:
+    """Tokens routed to each expert."""
+    return np.bincount(np.asarray(idx).reshape(-1), minlength=n_experts).astype(np.int32)
+
+
+def permutation(idx: np.ndarray, n_experts: int):
+    """Per-expert segments of the (token, k) pairs: a stable counting sort by expert of
+    the pairs in (t, k) order.  Implied by "GroupedExperts packs experts in groups"
+    ([K3-news] ¶"从代码结构看").
+
+    Returns offsets [E + 1], perm [bt*K] (slot -> token), inv [bt, K] ((t, k) -> slot)."""
+    idx = np.asarray(idx, np.int64)
+    bt, top_k = idx.shape
+    flat = idx.reshape(-1)
+    order = np.argsort(flat, kind="stable")           # pair ids sorted by expert, stable
+    counts = np.bincount(flat, minlength=n_experts)
+    offsets = np.zeros(n_experts + 1, np.int64)
+    offsets[1:] = np.cumsum(counts)
+    perm = (order // top_k).astype(np.int32)
+    inv = np.empty(bt * top_k, np.int64)
+    inv[order] = np.arange(bt * top_k)
+    return offsets.astype(np.int32), perm, inv.reshape(bt, top_k).astype(np.int32)
+
+
+def route(logits: np.ndarray, top_k: int) -> dict:
+    """The whole router on given logits (which already hold any bias): sigmoid scores,
+    per-expert cutoffs, top-K, combine weights, counts and segments.
+
+    Also reports `min_gap`: the smallest non-zero difference between adjacent keys among
+    each token's K+1 largest.  A selection computed elsewhere from the same logits in
+    fp64 agrees with this one whenever that gap exceeds both sides' rounding of sigmoid."""
+    l = np.asarray(logits, np.float64)
+    bt, n_experts = l.shape
+    s = sigmoid(l)
+    alpha = quantile_cutoff(s, top_k)
+    idx, sorted_keys = topk_select(s, alpha, top_k)
+    w = combine_weights(s, idx)
+    counts = expert_counts(idx, n_experts)
+    offsets, perm, inv = permutation(idx, n_experts)
+    m = min(top_k + 1, n_experts)
+    if bt > 0 and m > 1:
+        adj = sorted_keys[:, : m - 1] - sorted_keys[:, 1:m]
+        nz = adj[adj > 0]
+        min_gap = float(nz.min()) if nz.size else np.inf
+        exact_ties = int((adj == 0).sum())
+    else:
+        min_gap, exact_ties = np.inf, 0
+    return dict(s=s, alpha=alpha, idx=idx, w=w, counts=counts, offsets=offsets,
+                perm=perm, inv=inv, min_gap=min_gap, exact_ties=exact_ties)
+
+
+# --------------------------------------------------------------------------- experts
+
+def situ_glu(g: np.ndarray, u: np.ndarray, beta: float = 4.0, beta_u: float = 25.0) -> np.ndarray:
+    """SiTU-GLU, reading A1 of [K3-news] ¶"第一" (sigmoid-limited gate, tanh-bounded up
+    branch, upper bound): act = g' * sigmoid(g') * u', g' = beta tanh(g / beta),
+    u' = beta_u tanh(u / beta_u).  |act| < beta * sigmoid(beta) * beta_u."""
+    g = np.asarray(g, np.float64)
+    u = np.asarray(u, np.float64)
+    gp = beta * np.tanh(g / beta)
+    up = beta_u * np.tanh(u / beta_u)
+    return gp * sigmoid(gp) * up
+
+
+def rms_norm(y: np.ndarray, gamma: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    """latent_norm on each row: gamma * y / sqrt(mean(y^2) + eps) ([K3-news] ¶"第二":
+    RMSNorm moved to the latent output, before up_proj)."""
+    y = np.asarray(y, np.float64)
+    ms = np.mean(y * y, axis=-1, keepdims=True)
+    return np.asarray(gamma, np.float64) * y / np.sqrt(ms + eps)
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+def routed_latent(z: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float,
+                  beta_u: float, eps: float) -> np.ndarray:
+    """c[t] = sum_k w[t, k] * RMSNorm(W_d[e] act(W_g[e] z_t, W_u[e] z_t)), e = idx[t, k]:
+    the GroupedExperts at latent width followed by latent_norm and the weighted fusion
+    ([K3-news] ¶"具体前向流程"; [K3-arch] step e).  Tokens are grouped by expert only so
+    each expert's weights are read once; every (t, k) term is the same matrix-vector work."""
+    z = _f64(z)
+    n, latent = z.shape
+    c = np.zeros((n, latent))
+    gamma = _f64(weights["latent_gamma"])
+    for e in np.unique(idx):
+        rows, ks = np.nonzero(idx == e)
+        wg = _f64(weights["exp_gate"][int(e)])
+        wu = _f64(weights["exp_up"][int(e)])
+        wd = _f64(weights["exp_down"][int(e)])
+        zr = z[rows]
+        a = situ_glu(zr @ wg.T, zr @ wu.T, beta, beta_u)
+        yhat = rms_norm(a @ wd.T, gamma, eps)
+        c[rows] += _f64(w)[rows, ks][:, None] * yhat
+    return c
+
+
+def shared_experts(x: np.ndarray, weights, beta: float, beta_u: float) -> np.ndarray:
+    """sum_j W_d^sh[j] act(W_g^sh[j] x, W_u^sh[j] x): the always-active full-width
+    SiTU-GLU experts ([K3-news] ¶"具体前向流程": the shared branch; [K3-arch] step g)."""
+    x = _f64(x)
+    out = np.zeros((x.shape[0], _f64(weights["sh_down"][0]).shape[0]))
+    for j in range(len(weights["sh_down"])):
+        a = situ_glu(x @ _f64(weights["sh_gate"][j]).T, x @ _f64(weights["sh_up"][j]).T, beta, beta_u)
+        out += a @ _f64(weights["sh_down"][j]).T
+    return out
+
+
+def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float = 4.0,
+                  beta_u: float = 25.0, eps: float = 1e-6, return_parts: bool = False):
+    """Stable LatentMoE layer output for the rows of x, given their routing (idx, w).
+
+    out = W_up c + shared(x),  c = routed_latent(W_down x)  ([K3-news] ¶"具体前向流程":
+    two parallel paths from the flattened x; [K3-arch] steps d-g: W_down 7168 -> 3584,
+    16 experts at 3584, RMSNorm + W_up 3584 -> 7168, 2 shared experts at 7168).
+
+    `weights` maps names to arrays (or to lazily indexed per-expert providers for the
+    expert tensors): w_down [L, d], exp_gate / exp_up [E, I, L], exp_down [E, L, I],
+    latent_gamma [L], w_up [d, L], sh_gate / sh_up [S, Is, d], sh_down [S, d, Is]."""
+    x = _f64(x)
+    z = x @ _f64(weights["w_down"]).T
+    c = routed_latent(z, idx, w, weights, beta, beta_u, eps)
+    routed = c @ _f64(weights["w_up"]).T
+    shared = shared_experts(x, weights, beta, beta_u)
+    out = routed + shared
+    if return_parts:
+        return out, dict(z=z, c=c, routed=routed, shared=shared)
+    return out
+
+
+def forward(x: np.ndarray, weights, top_k: int, router_bias=None, logits=None, beta: float = 4.0,
+            beta_u: float = 25.0, eps: float = 1e-6) -> tuple[np.ndarray, dict]:
+    """Whole layer: route on `logits` if given (e.g. another implementation's fp32 logits,
+    upcast exactly), else on this oracle's own fp64 logits; then layer_forward."""
+    if logits is None:
+        logits = router_logits(x, weights["w_router"], router_bias)
+    r = route(logits, top_k)
+    out = layer_forward(x, r["idx"], r["w"], weights, beta, beta_u, eps)
+    return out, r

@@ -1,0 +1,89 @@
+"""Planted mistakes in the oracle (on the CPU): each plausible slip must make at least
+one pin fail, which shows the pins would catch it."""
+import numpy as np
+import pytest
+
+from oracle import lmoe_oracle as O
+import tests.test_oracle_pins as P
+
+
+def _fails(fn):
+    try:
+        fn()
+    except AssertionError:
+        return True
+    return False
+
+
+def test_dropped_sigmoid_in_situ_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "situ_glu", lambda g, u, beta=4.0, beta_u=25.0:
+                        beta * np.tanh(np.asarray(g) / beta) * beta_u * np.tanh(np.asarray(u) / beta_u))
+    assert _fails(P.test_situ_glu_reduces_to_swiglu)
+    assert _fails(P.test_forward_matches_brute_force)
+
+
+def test_swapped_bounds_in_situ_is_caught(monkeypatch):
+    orig = O.situ_glu
+    monkeypatch.setattr(O, "situ_glu", lambda g, u, beta=4.0, beta_u=25.0: orig(g, u, beta_u, beta))
+    assert _fails(P.test_situ_glu_bound_and_saturation)
+
+
+def test_quantile_off_by_one_is_caught(monkeypatch):
+    orig = O.quantile_position
+    monkeypatch.setattr(O, "quantile_position", lambda bt, E, K: (min(orig(bt, E, K)[0] + 1, bt - 1), orig(bt, E, K)[1]))
+    assert _fails(lambda: P.test_quantile_matches_torch_and_numpy(64, 16, 4))
+    assert _fails(P.test_quantile_count_invariant_random_columns)
+
+
+def test_quantile_wrong_direction_is_caught(monkeypatch):
+    # q = K/E instead of 1 - K/E
+    monkeypatch.setattr(O, "quantile_position", lambda bt, E, K: (((bt - 1) * K) // E, ((bt - 1) * K % E) / E))
+    assert _fails(lambda: P.test_quantile_matches_torch_and_numpy(2048, 64, 8))
+
+
+def test_rmsnorm_sum_instead_of_mean_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "rms_norm", lambda y, gamma, eps=1e-6:
+                        np.asarray(gamma) * y / np.sqrt((np.asarray(y) ** 2).sum(-1, keepdims=True) + eps))
+    assert _fails(P.test_rms_norm_matches_torch_and_has_unit_rms)
+    assert _fails(P.test_forward_matches_brute_force)
+
+
+def test_weights_from_keys_instead_of_scores_is_caught(monkeypatch):
+    def bad_route(logits, top_k, _orig=O.route):
+        r = _orig(logits, top_k)
+        keys = np.take_along_axis(r["s"] - r["alpha"][None], r["idx"].astype(np.int64), 1)
+        r["w"] = keys / keys.sum(1, keepdims=True)
+        return r
+    monkeypatch.setattr(O, "route", bad_route)
+    assert _fails(P.test_forward_matches_brute_force)
+
+
+def test_tie_break_to_higher_index_is_caught(monkeypatch):
+    def bad_topk(s, alpha, top_k):
+        keys = np.asarray(s) - np.asarray(alpha)[None, :]
+        E = keys.shape[1]
+        order = np.lexsort((-np.broadcast_to(np.arange(E), keys.shape), -keys), axis=-1)
+        return order[:, :top_k].astype(np.int32), np.take_along_axis(keys, order, -1)
+    monkeypatch.setattr(O, "topk_select", bad_topk)
+    assert _fails(P.test_topk_ties_go_to_lower_index)
+
+
+def test_swapped_shared_gate_and_up_is_caught(monkeypatch):
+    def bad_shared(x, weights, beta, beta_u):
+        W = dict(weights)
+        W["sh_gate"], W["sh_up"] = weights["sh_up"], weights["sh_gate"]
+        return O.__dict__["_orig_shared"](x, W, beta, beta_u)
+    monkeypatch.setitem(O.__dict__, "_orig_shared", O.shared_experts)
+    monkeypatch.setattr(O, "shared_experts", bad_shared)
+    assert _fails(P.test_forward_matches_brute_force)
+
+
+def test_unstable_segments_are_caught(monkeypatch):
+    def bad_perm(idx, E, _orig=O.permutation):
+        off, perm, inv = _orig(idx, E)
+        perm = perm.copy()
+        for e in range(E):           # reverse token order inside each expert segment
+            perm[off[e]:off[e + 1]] = perm[off[e]:off[e + 1]][::-1]
+        return off, perm, inv
+    monkeypatch.setattr(O, "permutation", bad_perm)
+    assert _fails(lambda: P.test_topk_and_segments_brute_force(64, 16, 4))

@@ -1,0 +1,378 @@
+"""Pins of the fp64 oracle to facts outside itself: the pages' printed parameter
+budget, library routines (torch.quantile, numpy.quantile, torch rms_norm, silu),
+closed forms, invariants and brute force on tiny inputs.  CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+from oracle import lmoe_oracle as O
+from workloads import WORKLOADS, LayerShape, Workload, make_inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _np(t):
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def _weights_np(weights):
+    return {k: _np(v) for k, v in weights.items()}
+
+
+# ----------------------------------------------------------------- parameter budget
+
+def test_param_budget_matches_printed_table():
+    g = json.load(open(os.path.join(GOLDEN, "param_budget.json")))
+    sh = g["shape"]
+    pc = O.param_counts(sh["d"], sh["latent"], sh["n_experts"], sh["top_k"], 3072, sh["n_shared"], 3072)
+    p = g["printed"]
+
+    def rounded(v, digits):
+        return round(v, digits)
+
+    assert rounded(pc["per_expert"] / 1e6, 1) == p["per_expert_M"]["value"]
+    assert rounded(pc["experts_total"] / 1e9, 1) == p["experts_total_G"]["value"]
+    assert rounded(pc["experts_active"] / 1e6, 0) == p["experts_active_M"]["value"]
+    assert rounded(pc["shared_total"] / 1e6, 0) == p["shared_total_M"]["value"]
+    assert rounded(pc["w_down"] / 1e6, 1) == p["w_down_M"]["value"]
+    assert rounded(pc["w_up"] / 1e6, 1) == p["w_up_M"]["value"]
+    assert rounded((pc["w_down"] + pc["w_up"]) / 1e6, 0) == p["w_down_plus_up_M"]["value"]
+    assert rounded(pc["router"] / 1e6, 1) == p["router_M"]["value"]
+    dense = O.param_counts(sh["d"], sh["latent"], 1, 1, 1, 1, sh["dense_ffn_inter"])["per_shared"]
+    assert rounded(dense / 1e6, 0) == p["dense_ffn_M"]["value"]
+    assert sh["top_k"] / sh["n_experts"] < p["active_fraction_below"]["value"]
+    # exact values used elsewhere (A13: intermediate 3072)
+    assert pc["per_expert"] == 33_030_144 and pc["per_shared"] == 66_060_288
+    assert pc["w_down"] == 25_690_112 and pc["router"] == 6_422_528
+
+
+# ----------------------------------------------------------------- quantile cutoff
+
+@pytest.mark.parametrize("bt,E,K", [(64, 16, 4), (2048, 64, 8), (1000, 896, 16), (7, 5, 2), (1, 4, 1), (2, 3, 3)])
+def test_quantile_matches_torch_and_numpy(bt, E, K):
+    rng = np.random.default_rng(bt * 31 + E)
+    s = O.sigmoid(rng.normal(size=(bt, E)) * 2)
+    a = O.quantile_cutoff(s, K)
+    q = 1.0 - K / E
+    ref_t = torch.quantile(torch.from_numpy(s), q, dim=0, interpolation="linear").numpy()
+    ref_n = np.quantile(s, q, axis=0, method="linear")
+    np.testing.assert_allclose(a, ref_t, rtol=4e-16, atol=1e-17)
+    np.testing.assert_allclose(a, ref_n, rtol=4e-16, atol=1e-17)
+
+
+@pytest.mark.parametrize("name,expected", [("tiny_f32", 16), ("small_bf16", 256),
+                                           ("full_prefill_bt8192", 147), ("full_decode_bt64", 2)])
+def test_quantile_count_invariant(name, expected):
+    """In a tie-free column exactly bt-1-floor(h) scores exceed alpha, which is within 1
+    of the load target bt*K/E ([K3-news] Quantile Balancing)."""
+    w = WORKLOADS[name]
+    s_, bt = w.shape, w.bt
+    j, _ = O.quantile_position(bt, s_.n_experts, s_.top_k)
+    assert bt - 1 - j == expected
+    assert abs(expected - bt * s_.top_k / s_.n_experts) <= 1.0
+
+
+def test_quantile_count_invariant_random_columns():
+    rng = np.random.default_rng(11)
+    for bt, E, K in [(64, 16, 4), (2048, 64, 8), (333, 40, 7)]:
+        s = O.sigmoid(rng.normal(size=(bt, E)))
+        a = O.quantile_cutoff(s, K)
+        above = (s > a[None, :]).sum(axis=0)
+        # closed form: bt-1-floor((bt-1)(E-K)/E) = ceil((bt-1)K/E)
+        expected = -((-(bt - 1) * K) // E)
+        assert np.all(above == expected)
+        assert np.all(np.abs(above - bt * K / E) <= 1.0)
+
+
+def test_quantile_special_cases():
+    rng = np.random.default_rng(3)
+    s = O.sigmoid(rng.normal(size=(50, 6)))
+    # K = E: q = 0, the cutoff is the column minimum
+    np.testing.assert_array_equal(O.quantile_cutoff(s, 6), s.min(axis=0))
+    # one token: the cutoff is that token's score
+    np.testing.assert_array_equal(O.quantile_cutoff(s[:1], 2), s[0])
+    # all-equal column: the cutoff is the shared value
+    c = np.full((9, 3), 0.25)
+    np.testing.assert_array_equal(O.quantile_cutoff(c, 1), np.full(3, 0.25))
+
+
+# ----------------------------------------------------------------- top-K, weights, segments
+
+def _brute_topk(keys, K):
+    out = []
+    for row in keys:
+        order = sorted(range(len(row)), key=lambda e: (-row[e], e))
+        out.append(order[:K])
+    return np.array(out, dtype=np.int32)
+
+
+def _brute_perm(idx, E):
+    bt, K = idx.shape
+    perm, inv = [], np.zeros((bt, K), np.int32)
+    offsets = [0]
+    for e in range(E):
+        for t in range(bt):
+            for k in range(K):
+                if idx[t, k] == e:
+                    inv[t, k] = len(perm)
+                    perm.append(t)
+        offsets.append(len(perm))
+    return np.array(offsets, np.int32), np.array(perm, np.int32), inv
+
+
+@pytest.mark.parametrize("bt,E,K", [(64, 16, 4), (37, 11, 3), (5, 8, 8), (20, 9, 1)])
+def test_topk_and_segments_brute_force(bt, E, K):
+    rng = np.random.default_rng(bt + 100 * E)
+    l = rng.normal(size=(bt, E))
+    l[3 % bt] = l[0]                       # a repeated token
+    r = O.route(l, K)
+    keys = r["s"] - r["alpha"][None, :]
+    np.testing.assert_array_equal(r["idx"], _brute_topk(keys, K))
+    # weights: the chosen raw scores over their sum, positive, summing to 1
+    for t in range(bt):
+        ch = [r["s"][t, e] for e in r["idx"][t]]
+        np.testing.assert_allclose(r["w"][t], np.array(ch) / sum(ch), rtol=1e-15)
+    assert np.all(r["w"] > 0)
+    np.testing.assert_allclose(r["w"].sum(axis=1), 1.0, rtol=1e-14)
+    assert r["counts"].sum() == bt * K
+    np.testing.assert_array_equal(r["counts"], np.bincount(r["idx"].ravel(), minlength=E))
+    off, perm, inv = _brute_perm(r["idx"], E)
+    np.testing.assert_array_equal(r["offsets"], off)
+    np.testing.assert_array_equal(r["perm"], perm)
+    np.testing.assert_array_equal(r["inv"], inv)
+
+
+def test_topk_ties_go_to_lower_index():
+    l = np.zeros((4, 10))                  # x = 0: every key is exactly 0
+    r = O.route(l, 3)
+    np.testing.assert_array_equal(r["idx"], np.tile(np.arange(3, dtype=np.int32), (4, 1)))
+    np.testing.assert_array_equal(r["w"], np.full((4, 3), 1 / 3))
+    assert r["exact_ties"] > 0
+
+
+def test_topk_k_equals_e_takes_every_expert():
+    rng = np.random.default_rng(9)
+    l = rng.normal(size=(30, 7))
+    r = O.route(l, 7)
+    np.testing.assert_array_equal(np.sort(r["idx"], axis=1), np.tile(np.arange(7), (30, 1)))
+    np.testing.assert_array_equal(r["alpha"], r["s"].min(axis=0))
+    s_sorted = np.take_along_axis(r["s"], r["idx"].astype(np.int64), axis=1)
+    np.testing.assert_allclose(r["w"], s_sorted / r["s"].sum(axis=1, keepdims=True), rtol=1e-15)
+
+
+# ----------------------------------------------------------------- SiTU-GLU and RMSNorm
+
+def test_situ_glu_bound_and_saturation():
+    v = np.concatenate([-np.logspace(-6, 4, 200), [0.0], np.logspace(-6, 4, 200)])
+    g, u = np.meshgrid(v, v)
+    a = O.situ_glu(g, u)
+    bound = 4.0 / (1.0 + math.exp(-4.0)) * 25.0       # beta * sigmoid(beta) * beta_u
+    assert np.all(np.abs(a) <= bound) and bound < 4.0 * 25.0
+    np.testing.assert_allclose(O.situ_glu(1e4, 1e4), bound, rtol=1e-15)
+    np.testing.assert_allclose(O.situ_glu(1e4, -1e4), -bound, rtol=1e-15)
+    # far negative gate: g' -> -beta, sigmoid(-beta) * (-beta)
+    np.testing.assert_allclose(O.situ_glu(-1e4, 1e4), -4.0 / (1 + math.exp(4.0)) * 25.0, rtol=1e-14)
+
+
+def test_situ_glu_reduces_to_swiglu():
+    """With very large beta and beta_u the bounds vanish and SiTU-GLU is SwiGLU silu(g)*u."""
+    rng = np.random.default_rng(1)
+    g, u = rng.normal(size=1000) * 5, rng.normal(size=1000) * 5
+    ref = (F.silu(torch.from_numpy(g)) * torch.from_numpy(u)).numpy()
+    np.testing.assert_allclose(O.situ_glu(g, u, 1e8, 1e8), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_situ_glu_symmetries_and_small_argument():
+    rng = np.random.default_rng(2)
+    g, u = rng.normal(size=100), rng.normal(size=100)
+    assert np.all(O.situ_glu(0.0, u) == 0.0)
+    np.testing.assert_array_equal(O.situ_glu(g, -u), -O.situ_glu(g, u))      # odd in u
+    # near zero: g' ~ g, sigmoid(g') ~ 1/2, u' ~ u  =>  act ~ g u / 2
+    e = 1e-6
+    np.testing.assert_allclose(O.situ_glu(e * g, e * u), e * e * g * u / 2, rtol=1e-5)
+    # the two bounds act on their own arguments: swapping beta and beta_u changes the result
+    assert not np.allclose(O.situ_glu(3 * g, 3 * u, 4, 25), O.situ_glu(3 * g, 3 * u, 25, 4))
+
+
+def test_rms_norm_matches_torch_and_has_unit_rms():
+    rng = np.random.default_rng(4)
+    y = rng.normal(size=(50, 64)) * rng.uniform(0.01, 100, size=(50, 1))
+    gamma = 1 + 0.1 * rng.normal(size=64)
+    ref = F.rms_norm(torch.from_numpy(y), (64,), torch.from_numpy(gamma), eps=1e-6).numpy()
+    np.testing.assert_allclose(O.rms_norm(y, gamma, 1e-6), ref, rtol=1e-13, atol=1e-15)
+    unit = O.rms_norm(y, np.ones(64), 0.0)
+    np.testing.assert_allclose(np.sqrt((unit ** 2).mean(axis=1)), 1.0, rtol=1e-12)
+    np.testing.assert_allclose(O.rms_norm(7.0 * y, gamma, 0.0), O.rms_norm(y, gamma, 0.0), rtol=1e-12)
+
+
+# ----------------------------------------------------------------- whole layer
+
+def _tiny(seed=0, **kw):
+    shape = LayerShape(d=32, latent=16, n_experts=6, top_k=2, expert_inter=24, n_shared=2, shared_inter=20,
+                       dtype="f32")
+    w = Workload("pin", shape, 12, seed, **kw)
+    x, weights, bias = make_inputs(w, "cpu")
+    return shape, _np(x), _weights_np(weights), (None if bias is None else _np(bias))
+
+
+def _brute_forward(x, weights, shape, logits):
+    """Per-token loops over explicit dot products; no grouping, no vectorised routing."""
+    bt, E, K = x.shape[0], shape.n_experts, shape.top_k
+    s = [[1 / (1 + math.exp(-logits[t][e])) for e in range(E)] for t in range(bt)]
+    j = ((bt - 1) * (E - K)) // E
+    frac = ((bt - 1) * (E - K) - j * E) / E
+    alpha = []
+    for e in range(E):
+        col = sorted(s[t][e] for t in range(bt))
+        alpha.append(col[j] + frac * (col[j + 1] - col[j]) if j + 1 < bt else col[j])
+
+    def act(gv, uv):
+        gp = shape.beta * math.tanh(gv / shape.beta)
+        up = shape.beta_u * math.tanh(uv / shape.beta_u)
+        return gp / (1 + math.exp(-gp)) * up
+
+    def matvec(W, v):
+        return [sum(W[r][i] * v[i] for i in range(len(v))) for r in range(len(W))]
+
+    out = np.zeros((bt, shape.d))
+    for t in range(bt):
+        keys = [s[t][e] - alpha[e] for e in range(E)]
+        chosen = sorted(range(E), key=lambda e: (-keys[e], e))[:K]
+        tot = sum(s[t][e] for e in chosen)
+        z = matvec(weights["w_down"], x[t])
+        c = [0.0] * shape.latent
+        for e in chosen:
+            g = matvec(weights["exp_gate"][e], z)
+            u = matvec(weights["exp_up"][e], z)
+            a = [act(g[i], u[i]) for i in range(len(g))]
+            y = matvec(weights["exp_down"][e], a)
+            rms = math.sqrt(sum(v * v for v in y) / len(y) + shape.rms_eps)
+            for i in range(len(y)):
+                c[i] += s[t][e] / tot * weights["latent_gamma"][i] * y[i] / rms
+        o = matvec(weights["w_up"], c)
+        for jsh in range(shape.n_shared):
+            g = matvec(weights["sh_gate"][jsh], x[t])
+            u = matvec(weights["sh_up"][jsh], x[t])
+            a = [act(g[i], u[i]) for i in range(len(g))]
+            o = [o[i] + v for i, v in enumerate(matvec(weights["sh_down"][jsh], a))]
+        out[t] = o
+    return out
+
+
+def test_forward_matches_brute_force():
+    shape, x, W, _ = _tiny(gamma_noise=0.1)
+    logits = O.router_logits(x, W["w_router"]) * 40.0   # spread scores so routing is not trivial
+    out, r = O.forward(x, W, shape.top_k, logits=logits)
+    ref = _brute_forward(x, W, shape, logits)
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_torch_library_formulation():
+    """The layer written with torch fp64 library routines (linear, sigmoid, quantile,
+    stable sort, rms_norm) instead of the oracle's numpy code."""
+    shape, x, W, _ = _tiny(seed=3, gamma_noise=0.1)
+    tx = torch.from_numpy(x)
+    TW = {k: torch.from_numpy(v) for k, v in W.items()}
+    logits = F.linear(tx, TW["w_router"]) * 40.0
+    s = torch.sigmoid(logits)
+    alpha = torch.quantile(s, 1 - shape.top_k / shape.n_experts, dim=0, interpolation="linear")
+    keys = s - alpha
+    # stable descending sort keeps the lower index first among equal keys
+    idx = torch.sort(keys, dim=1, descending=True, stable=True).indices[:, : shape.top_k]
+    ws = torch.gather(s, 1, idx)
+    ws = ws / ws.sum(1, keepdim=True)
+    z = F.linear(tx, TW["w_down"])
+
+    def act(g, u):
+        gp = shape.beta * torch.tanh(g / shape.beta)
+        return F.silu(gp) * shape.beta_u * torch.tanh(u / shape.beta_u)
+
+    c = torch.zeros(x.shape[0], shape.latent, dtype=torch.float64)
+    for k in range(shape.top_k):
+        for t in range(x.shape[0]):
+            e = int(idx[t, k])
+            y = F.linear(act(F.linear(z[t], TW["exp_gate"][e]), F.linear(z[t], TW["exp_up"][e])), TW["exp_down"][e])
+            c[t] += ws[t, k] * F.rms_norm(y, (shape.latent,), TW["latent_gamma"], eps=shape.rms_eps)
+    ref = F.linear(c, TW["w_up"])
+    for j in range(shape.n_shared):
+        ref += F.linear(act(F.linear(tx, TW["sh_gate"][j]), F.linear(tx, TW["sh_up"][j])), TW["sh_down"][j])
+    out, r = O.forward(x, W, shape.top_k, logits=logits.numpy())
+    np.testing.assert_array_equal(r["idx"], idx.numpy())
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_forward_zero_input_is_zero():
+    shape, x, W, _ = _tiny()
+    out, r = O.forward(np.zeros_like(x), W, shape.top_k)
+    assert np.all(out == 0.0)
+    np.testing.assert_array_equal(r["idx"], np.tile(np.arange(shape.top_k, dtype=np.int32), (x.shape[0], 1)))
+    np.testing.assert_array_equal(r["w"], np.full_like(r["w"], 1 / shape.top_k))
+
+
+def test_forward_single_expert_is_dense_latent_ffn():
+    """E = K = 1: routing is trivial and the layer is W_up RMSNorm(FFN(W_down x)) + shared."""
+    shape = LayerShape(d=24, latent=8, n_experts=1, top_k=1, expert_inter=12, n_shared=1, shared_inter=10,
+                       dtype="f32")
+    x, weights, _ = make_inputs(Workload("e1", shape, 9, 7, gamma_noise=0.2), "cpu")
+    x, W = _np(x), _weights_np(weights)
+    out, r = O.forward(x, W, 1)
+    assert np.all(r["idx"] == 0) and np.all(r["w"] == 1.0)
+    tx = torch.from_numpy(x)
+    TW = {k: torch.from_numpy(v) for k, v in W.items()}
+
+    def act(g, u):
+        gp = 4.0 * torch.tanh(g / 4.0)
+        return F.silu(gp) * 25.0 * torch.tanh(u / 25.0)
+
+    z = F.linear(tx, TW["w_down"])
+    y = F.linear(act(F.linear(z, TW["exp_gate"][0]), F.linear(z, TW["exp_up"][0])), TW["exp_down"][0])
+    ref = F.linear(F.rms_norm(y, (8,), TW["latent_gamma"], eps=1e-6), TW["w_up"])
+    ref += F.linear(act(F.linear(tx, TW["sh_gate"][0]), F.linear(tx, TW["sh_up"][0])), TW["sh_down"][0])
+    np.testing.assert_allclose(out, ref.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_up_projection_linearity():
+    """A11: W_up applied to the weighted latent sum equals the weighted sum of W_up y_k."""
+    shape, x, W, _ = _tiny(seed=5)
+    r = O.route(O.router_logits(x, W["w_router"]) * 40, shape.top_k)
+    z = x @ W["w_down"].T
+    c = O.routed_latent(z, r["idx"], r["w"], W, 4.0, 25.0, 1e-6)
+    per = np.zeros((x.shape[0], shape.d))
+    for t in range(x.shape[0]):
+        for k in range(shape.top_k):
+            e = r["idx"][t, k]
+            a = O.situ_glu(W["exp_gate"][e] @ z[t], W["exp_up"][e] @ z[t])
+            yk = O.rms_norm(W["exp_down"][e] @ a, W["latent_gamma"])
+            per[t] += r["w"][t, k] * (W["w_up"] @ yk)
+    np.testing.assert_allclose(c @ W["w_up"].T, per, rtol=1e-12, atol=1e-13)
+
+
+def test_forward_equivariances():
+    """Relabelling experts leaves outputs unchanged; permuting tokens permutes them."""
+    shape, x, W, _ = _tiny(seed=8)
+    logits = O.router_logits(x, W["w_router"]) * 40
+    out, _ = O.forward(x, W, shape.top_k, logits=logits)
+    p = np.random.default_rng(0).permutation(shape.n_experts)
+    W2 = dict(W)
+    for k in ("exp_gate", "exp_up", "exp_down"):
+        W2[k] = W[k][p]
+    out2, _ = O.forward(x, W2, shape.top_k, logits=logits[:, p])
+    np.testing.assert_allclose(out2, out, rtol=1e-13, atol=1e-13)
+    tp = np.random.default_rng(1).permutation(x.shape[0])
+    out3, _ = O.forward(x[tp], W, shape.top_k, logits=logits[tp])
+    np.testing.assert_allclose(out3, out[tp], rtol=1e-13, atol=1e-13)
+
+
+def test_zipf_and_repeated_block_recipe():
+    w = WORKLOADS["full_skewed_bt16384"]
+    assert w.zipf_bias and w.repeat_frac == 0.25
+    small = w.with_(shape=LayerShape(64, 32, 16, 4, 32, 2, 32), bt=40)
+    x, _, bias = make_inputs(small, "cpu")
+    assert torch.equal(x[:10], x[:1].expand(10, -1)) and not torch.equal(x[10], x[0])
+    ranks = torch.sort(bias, descending=True).values
+    np.testing.assert_allclose(ranks.numpy(), 3.0 * np.arange(1, 17, dtype=np.float64) ** -1.1, rtol=1e-6)
