@@ -1,0 +1,401 @@
+#!/usr/bin/env python3
+"""Stable LatentMoE layer forward throughput on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl lmoe|reference]
+                    [--workload NAME] [--cpu-tokens T] [--no-cpu-baseline]
+
+One step = one lmoe_forward (router GEMM, cutoffs, top-K, segments, W_down, grouped
+expert gate/up + SiTU-GLU, expert down, RMSNorm + combine, shared experts, W_up +
+shared down) over one synthetic batch already resident in HBM.  Prints one JSON line
+(rank 0).  N > 1 (torchrun) runs N independent replicas, one per GPU, each with its own
+batch: the cutoffs are per batch, so the layer has no data-parallel exchange step.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (each step a
+bounded sample of the same workload); it is a deliberately slow correctness program."""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from workloads import WORKLOADS, make_inputs, make_x  # noqa: E402
+
+DEFAULT_WORKLOAD = "full_prefill_bt8192"
+METRIC = "LatentMoE layer fwd tokens/s on 1 B300; % of bf16 TC peak (or HBM BW)"
+
+
+# ----------------------------------------------------------------------------- arithmetic
+
+def algorithmic(shape, bt, n_touched):
+    """Algorithmic FLOPs and bytes of one layer call and of each stage (2*M*N*K per GEMM;
+    bytes = what each stage must read and write at least once).  n_touched = experts
+    with at least one token."""
+    d, L, E, K, I, S, Is = (shape.d, shape.latent, shape.n_experts, shape.top_k, shape.expert_inter,
+                            shape.n_shared, shape.shared_inter)
+    b = 2 if shape.dtype == "bf16" else 4
+    st = {
+        "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
+        "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
+        "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
+        "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, (n_touched * 2 * I * L + bt * K * L + bt * K * I) * b),
+        "expert_down_gemm": (2 * bt * K * L * I, (n_touched * L * I + bt * K * I + bt * K * L) * b),
+        "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),
+        "shared_gate_up_gemm": (2 * bt * S * 2 * Is * d, (S * 2 * Is * d + bt * d + bt * S * Is) * b),
+        "up_shared_down_gemm": (2 * bt * d * (L + S * Is), (d * (L + S * Is) + bt * (L + S * Is) + bt * d) * b),
+    }
+    flops = 2 * bt * (E * d + L * d + K * 3 * L * I + d * L + S * 3 * d * Is)
+    weight_bytes = (E * d + 2 * L * d + L + n_touched * 3 * L * I + S * 3 * d * Is) * b
+    layer_bytes = weight_bytes + 2 * bt * d * b
+    return flops, layer_bytes, st
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm=j["hbm_gbs"], tc=j["bf16_tflops"], tc_sustained=j["bf16_tflops_sustained"],
+                    source="measured")
+    return dict(hbm=6400.0, tc=1800.0, tc_sustained=1400.0, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons of this process's GPU, sampled every 100 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        pr = torch.cuda.get_device_properties(device)
+        self.bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            self.path = f"/tmp/lmoe_clocks_{os.getpid()}.csv"
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self.bus, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[0]) for r in rows]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(num(r[1]) for r in rows),
+                "power_w_max": max(num(r[2]) for r in rows), "samples": len(rows),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    return ws, rank, local
+
+
+def barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(v: float, ws: int, device) -> float:
+    if ws == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(v: float, ws: int, device) -> float:
+    if ws == 1:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def _blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        info = threadpool_info()
+        n = [i.get("num_threads", 0) for i in info if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_time(w, x, weights, bias, n_tokens: int, offset: int = 0):
+    """Wall time of the fp64 oracle on n_tokens tokens of the batch (routing over those
+    tokens, then the layer), fetching each needed expert's weights from device memory
+    and upcasting them as it goes (the oracle's weight source)."""
+    from oracle import lmoe_oracle as O
+
+    class PerIndex:
+        def __init__(self, t):
+            self.t = t
+
+        def __getitem__(self, i):
+            return self.t[int(i)].cpu().to(torch.float64).numpy()
+
+        def __len__(self):
+            return self.t.shape[0]
+
+    bt = x.shape[0]
+    rows = (np.arange(n_tokens) * max(1, bt // n_tokens) + offset) % bt
+    xs = x[torch.as_tensor(rows, device=x.device)].cpu().to(torch.float64).numpy()
+    t0 = time.perf_counter()
+    W = {k: (PerIndex(v) if v.dim() == 3 else v.cpu().to(torch.float64).numpy()) for k, v in weights.items()}
+    b = None if bias is None else bias.cpu().to(torch.float64).numpy()
+    s = w.shape
+    O.forward(xs, W, s.top_k, router_bias=b, beta=s.beta, beta_u=s.beta_u, eps=s.rms_eps)
+    return time.perf_counter() - t0
+
+
+# ----------------------------------------------------------------------------- traffic record
+
+def kernel_traffic(stage: str):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, if the kernel source
+    it was taken from is unchanged (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(stage)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
+        return None
+    return rec["dram_bytes_per_launch"]
+
+
+# ----------------------------------------------------------------------------- main
+
+def run_reference(args, ws, rank):
+    """The oracle as the reference arm: rank 0 only."""
+    if rank != 0:
+        return 0
+    w = WORKLOADS[args.workload]
+    device = torch.device("cuda", 0) if torch.cuda.is_available() else torch.device("cpu")
+    x, weights, bias = make_inputs(w, device)
+    n = args.cpu_tokens_ref
+    for i in range(args.warmup):
+        oracle_sample_time(w, x, weights, bias, n, offset=i)
+    total = 0.0
+    for i in range(args.steps):
+        total += oracle_sample_time(w, x, weights, bias, n, offset=args.warmup + i)
+    value = n * args.steps / total
+    cores = _blas_threads()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "bt": w.bt, "d": w.shape.d, "latent": w.shape.latent,
+                       "n_experts": w.shape.n_experts, "top_k": w.shape.top_k,
+                       "expert_inter": w.shape.expert_inter, "n_shared": w.shape.n_shared,
+                       "shared_inter": w.shape.shared_inter, "parallelism": "single process, host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} tokens of the batch per step (routing over the sample), "
+                                       "expert weights fetched from HBM and upcast inside the timing"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="lmoe", choices=["lmoe", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-tokens", type=int, default=12, help="oracle sample for cpu_baseline")
+    ap.add_argument("--cpu-tokens-ref", type=int, default=2, help="oracle sample per reference step")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        rc = run_reference(args, ws, rank)
+        barrier(ws)
+        return rc
+
+    from sparse_moe_layer_cutoff_b300 import LatentMoE
+    from sparse_moe_layer_cutoff_b300.lmoe import lmoe_build_info, lmoe_profile, lmoe_profile_read
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = WORKLOADS[args.workload]
+    s = w.shape
+    x, weights, bias = make_inputs(w, device)
+    xs = [x, make_x(w, device, seed_offset=1 + rank)]
+    layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias)
+    out = torch.empty((w.bt, s.d), dtype=layer.dtype, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    # experts touched (for the algorithmic byte count), from the route of each batch
+    touched = []
+    for xb in xs:
+        r = layer.route(xb)
+        touched.append(int((r["counts"] > 0).sum().item()))
+    n_touched = sum(touched) / len(touched)
+
+    for i in range(args.warmup):
+        layer.forward(xs[i % 2], out)
+    torch.cuda.synchronize()
+    if layer.sync_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    lmoe_profile(layer.ctx, True)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        layer.forward(xs[i % 2], out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    lmoe_profile(layer.ctx, False)
+    barrier(ws)
+    ms_local = e0.elapsed_time(e1)
+    st, stage_ms, calls, launches = lmoe_profile_read(layer.ctx)
+    status = layer.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    ms = max_over_ranks(ms_local, ws, device)
+    tokens_all = sum_over_ranks(float(w.bt * args.steps), ws, device)
+    value = tokens_all / (ms / 1e3)
+
+    # ---- roofline of the dominant kernel (largest share of the timed region)
+    pk = peaks()
+    flops, layer_bytes, per_stage = algorithmic(s, w.bt, n_touched)
+    dom = max(stage_ms, key=lambda k: stage_ms[k])
+    dom_ms = stage_ms[dom] / max(calls, 1)
+    f, b = per_stage[dom]
+    long_step = ms / 1e3 > 2.0
+    tc_peak = pk["tc_sustained"] if long_step else pk["tc"]
+    if f / (tc_peak * 1e12) > b / (pk["hbm"] * 1e9):
+        roof = {"bound": "tensor", "achieved": f / (dom_ms / 1e3) / 1e12, "peak": tc_peak, "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": b / (dom_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(dom)
+    roof.update({"kernel": dom, "ms_per_launch": dom_ms, "algorithmic_flops": f, "algorithmic_bytes": b,
+                 "peak_source": pk["source"] + (" sustained" if (roof["bound"] == "tensor" and long_step) else
+                                                " burst" if roof["bound"] == "tensor" else "")})
+    step_s = ms / 1e3 / args.steps
+    layer_roof = {"tflops": flops / step_s / 1e12, "tc_frac": flops / step_s / 1e12 / pk["tc"],
+                  "gbs": layer_bytes / step_s / 1e9, "hbm_frac": layer_bytes / step_s / 1e9 / pk["hbm"],
+                  "algorithmic_flops": flops, "algorithmic_bytes": layer_bytes, "experts_touched": n_touched}
+
+    # ---- end to end through the C ABI from pinned host buffers
+    xh = [t.cpu().pin_memory() for t in xs]
+    oh = torch.empty((w.bt, s.d), dtype=layer.dtype).pin_memory()
+    xd = torch.empty_like(x)
+    for i in range(2):
+        xd.copy_(xh[i], non_blocking=True)
+        layer.forward(xd, out)
+        oh.copy_(out, non_blocking=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for i in range(args.e2e_steps):
+        xd.copy_(xh[i % 2], non_blocking=True)
+        layer.forward(xd, out)
+        oh.copy_(out, non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3), ws, device)
+    e2e_value = sum_over_ranks(float(w.bt * args.e2e_steps), ws, device) / (e2e_ms / 1e3)
+    xbytes = w.bt * s.d * (2 if s.dtype == "bf16" else 4)
+
+    # ---- CPU oracle baseline (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        t = oracle_sample_time(w, x, weights, bias, args.cpu_tokens)
+        cpu = {"value": args.cpu_tokens / t, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
+               "sample": f"{args.cpu_tokens} tokens spread over the batch, routed among themselves, "
+                         f"{t:.1f} s wall; expert weights fetched from HBM and upcast to fp64 inside the timing"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": s.dtype, "data": "synthetic",
+                "config": {"workload": w.name, "bt": w.bt, "d": s.d, "latent": s.latent, "n_experts": s.n_experts,
+                           "top_k": s.top_k, "expert_inter": s.expert_inter, "n_shared": s.n_shared,
+                           "shared_inter": s.shared_inter, "global_batch": w.bt * ws,
+                           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                           "l2": "no flush: every step streams the whole weight set "
+                                 f"({layer_bytes / 1e9:.1f} GB algorithmic) through a 126 MB L2"},
+                "roofline": roof, "layer_roofline": layer_roof,
+                "stage_ms_per_step": {k: v / max(calls, 1) for k, v in stage_ms.items()},
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
+                        "d2h_bytes_per_step": xbytes},
+                "gpu_launches": launches, "clocks": clk, "engine": lmoe_build_info()}
+        print(json.dumps(line), flush=True)
+    layer.close()
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,187 @@
+/*
+ * lmoe.h -- C ABI of the Stable LatentMoE layer forward for one B300 (sm_103a).
+ *
+ * The layer ("KimiK3的StableLatentMoE架构解析", tech.news18a.com: ¶"从代码结构看" / Fig. 1 lists
+ * router, down_proj, experts, latent_norm, up_proj and shared; ¶"具体前向流程" / Fig. 2 gives
+ * the order), for a flattened batch x[bt, d]:
+ *
+ *   l      = x W_r^T (+ b)                      router logits, fp32          [bt, E]
+ *   s      = sigmoid(l)                                                       (fp64)
+ *   alpha_e = quantile_{1-K/E}(s[:, e])          Quantile Balancing cutoff    [E]   (fp64)
+ *   idx[t] = top-K of (s[t, :] - alpha), ties to the lower expert index, key-descending
+ *   w[t,k] = s[t, idx[t,k]] / sum_k' s[t, idx[t,k']]
+ *   z      = x W_down^T                          d -> latent
+ *   y_tk   = W_d[e] act(W_g[e] z_t, W_u[e] z_t)  e = idx[t,k]   (GroupedExperts, latent width)
+ *   c_t    = sum_k w[t,k] * gamma * y_tk / sqrt(mean(y_tk^2) + eps)   (latent_norm, weighted fusion)
+ *   out_t  = W_up c_t + sum_j W_d^sh[j] act(W_g^sh[j] x_t, W_u^sh[j] x_t)  (up_proj + 2 shared)
+ *
+ *   act(g, u) = g' sigmoid(g') u',  g' = beta tanh(g / beta),  u' = beta_u tanh(u / beta_u)
+ *   (SiTU-GLU, same page ¶"第一"; beta = 4, beta_u = 25).
+ *
+ * Shapes at the pages' size ("Vue d'ensemble de l'architecture", mkdocs.reaper.mx, sections
+ * "Le budget de paramètres" and "Par où l'information passe"): d = 7168, latent = 3584,
+ * E = 896, K = 16, 2 shared experts, intermediate 3072.
+ *
+ * Conventions for every call:
+ *   - Tensor arguments are DEVICE pointers on the current CUDA device, row-major, densely
+ *     packed, 16-byte aligned.  Weights are [out, in] (nn.Linear layout), so both GEMM
+ *     operands are K-major.  Element type = cfg.dtype (fp32 or bf16) unless stated.
+ *   - The caller owns x, out, every weight and every optional output buffer.  Weights are
+ *     borrowed: they are not copied and must stay valid and unchanged while the context
+ *     lives.  The context owns its workspace (allocated once, at create, for max_bt tokens).
+ *   - Calls are asynchronous and ordered on the given stream (a cudaStream_t; NULL = the
+ *     legacy default stream).  A context is used by one stream at a time; calls on two
+ *     streams that overlap race on the workspace.
+ *   - Errors are returned, never raised or printed: argument errors are found on the host
+ *     before any launch and nothing is launched; CUDA runtime errors map to LMOE_ERR_CUDA.
+ *     Kernels never trap: a device-side wait that runs out of time or an internal
+ *     inconsistency sets a status word that lmoe_sync_status() returns as
+ *     LMOE_ERR_TIMEOUT / LMOE_ERR_DEVICE_ASSERT.  With LMOE_CHECK=1 in the environment each
+ *     call synchronises its stream and returns that status itself.
+ *   - bt == 0 is valid and does nothing; bt > max_bt is LMOE_ERR_INVALID_ARG.
+ *   - Non-finite inputs give unspecified (but memory-safe) results.
+ */
+#ifndef LMOE_H
+#define LMOE_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LMOE_API __attribute__((visibility("default")))
+#else
+#define LMOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LMOE_OK = 0,
+  LMOE_ERR_INVALID_ARG = 1,   /* NULL / misaligned / host pointer, bad size, bt > max_bt       */
+  LMOE_ERR_UNSUPPORTED = 2,   /* valid layer, but outside what the kernels implement (below)  */
+  LMOE_ERR_OOM = 3,           /* workspace allocation failed at create                        */
+  LMOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed                          */
+  LMOE_ERR_TIMEOUT = 5,       /* a device-side bounded wait expired (kernel returned early)   */
+  LMOE_ERR_DEVICE_ASSERT = 6  /* a device-side consistency check failed                       */
+} lmoe_status;
+
+typedef enum { LMOE_F32 = 0, LMOE_BF16 = 1 } lmoe_dtype;
+
+/* Layer hyper-parameters.
+ * Supported: 1 <= top_k <= n_experts <= 4096, top_k <= 64, 1 <= n_shared <= 3.
+ * LMOE_BF16: d, latent, expert_inter, shared_inter multiples of 64 (tensor-core tiles).
+ * LMOE_F32 : latent a multiple of 4 (the fp32 path runs on CUDA cores, fp32 FMA).
+ * beta, beta_u > 0; rms_eps >= 0.  Anything else: LMOE_ERR_UNSUPPORTED / INVALID_ARG. */
+typedef struct {
+  int32_t d;             /* model width                                   (7168) */
+  int32_t latent;        /* latent width of the routed path               (3584) */
+  int32_t n_experts;     /* E, routed experts                             (896)  */
+  int32_t top_k;         /* K, experts per token                          (16)   */
+  int32_t expert_inter;  /* I, routed expert intermediate size            (3072) */
+  int32_t n_shared;      /* S, always-active shared experts               (2)    */
+  int32_t shared_inter;  /* Is, shared expert intermediate size           (3072) */
+  float beta;            /* SiTU-GLU gate bound                           (4)    */
+  float beta_u;          /* SiTU-GLU up-branch bound                      (25)   */
+  float rms_eps;         /* latent RMSNorm epsilon                        (1e-6) */
+  int32_t dtype;         /* lmoe_dtype of x, out and every weight               */
+} lmoe_config;
+
+/* Borrowed weight tensors (device pointers, dtype = cfg.dtype, row-major [out, in]). */
+typedef struct {
+  const void* w_router;      /* [E, d]                                                   */
+  const float* router_bias;  /* [E] fp32, added to the fp32 logits before sigmoid; NULL = none */
+  const void* w_down;        /* [latent, d]           W_down                              */
+  const void* latent_gamma;  /* [latent]              RMSNorm gain                        */
+  const void* w_up;          /* [d, latent]           W_up                                */
+  const void* exp_gate;      /* [E, I, latent]        routed expert gate                  */
+  const void* exp_up;        /* [E, I, latent]        routed expert up                    */
+  const void* exp_down;      /* [E, latent, I]        routed expert down                  */
+  const void* sh_gate;       /* [S, Is, d]            shared expert gate                  */
+  const void* sh_up;         /* [S, Is, d]            shared expert up                    */
+  const void* sh_down;       /* [S, d, Is]            shared expert down                  */
+} lmoe_weights;
+
+typedef struct lmoe_ctx lmoe_ctx;
+typedef void* lmoe_stream; /* a cudaStream_t */
+
+/* Validate cfg and weights, build the tensor-memory descriptors for the borrowed weights and
+ * allocate the workspace for up to max_bt tokens (about bt*K*(I + latent)*2 bytes plus
+ * O(bt*(E + d)) for bf16) on the current device.  Launches nothing; `stream` is only
+ * recorded as the context's default.  On success *out owns the context (free with
+ * lmoe_destroy); on any error *out is set to NULL and nothing stays allocated. */
+LMOE_API lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt,
+                        lmoe_stream stream, lmoe_ctx** out);
+
+/* The router alone ("QuantileBalancingRouter", ¶"具体前向流程" and ¶"第三" of the news18a
+ * page): logits, sigmoid scores, per-expert cutoffs, top-K, combine weights, per-expert
+ * counts and the per-expert token segments (kept in the workspace for lmoe_forward).
+ * x: [bt, d].  Every output pointer is an optional device buffer (NULL = not written):
+ *   topk_idx      [bt, K] int32   expert ids, key-descending, ties to the lower id
+ *   topk_w        [bt, K] fp32    combine weights (sum to 1 per token)
+ *   expert_counts [E]     int32   tokens per expert (sum = bt * K)
+ *   alpha         [E]     fp64    cutoffs
+ *   logits        [bt, E] fp32    router logits including router_bias
+ * Outputs are written in stream order; read them after synchronising the stream. */
+LMOE_API lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream,
+                       int32_t* topk_idx, float* topk_w, int32_t* expert_counts,
+                       double* alpha, float* logits);
+
+/* The whole layer: out[bt, d] (dtype = cfg.dtype) = routed path + shared path for x[bt, d].
+ * The cutoffs are computed over the bt tokens of this call (no state across calls, so a
+ * batch split into several calls routes differently).  out must not overlap x. */
+LMOE_API lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream);
+
+/* Synchronise `stream`, then return (and clear) the device status word of the context:
+ * LMOE_OK, LMOE_ERR_TIMEOUT or LMOE_ERR_DEVICE_ASSERT. */
+LMOE_API lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream);
+
+/* Synchronise the context's work, free its workspace and the context.  NULL is a no-op. */
+LMOE_API void lmoe_destroy(lmoe_ctx* ctx);
+
+/* Static, NUL-terminated name of a status code. */
+LMOE_API const char* lmoe_status_string(lmoe_status s);
+
+/* Read-only device pointers to the intermediates of the last route/forward call, for
+ * inspection and tests (valid until the next call or lmoe_destroy):
+ *   logits [bt, E] fp32, alpha [E] fp64, topk_idx/topk_w [bt, K], offsets [E + 1] int32
+ *   (expert segment starts in slot space), perm [bt*K] int32 (slot -> token),
+ *   inv [bt, K] int32 ((t, k) -> slot), z [bt, latent], h [bt*K, I] (slot-ordered expert
+ *   activations), y [bt*K, latent] (slot-ordered expert outputs), cat [bt, latent + S*Is]
+ *   (columns [0, latent) = c, then the S shared activations).  z, h, y, cat are cfg.dtype. */
+typedef struct {
+  int32_t bt;
+  const float* logits;
+  const double* alpha;
+  const int32_t* topk_idx;
+  const float* topk_w;
+  const int32_t* offsets;
+  const int32_t* perm;
+  const int32_t* inv;
+  const void* z;
+  const void* h;
+  const void* y;
+  const void* cat;
+} lmoe_workspace_view;
+
+LMOE_API lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* out);
+
+/* Per-stage device timing.  lmoe_profile(ctx, 1) clears the record and starts recording
+ * CUDA events on the call's stream at every stage boundary of each lmoe_forward (up to
+ * 1024 calls); lmoe_profile(ctx, 0) stops.  lmoe_profile_read synchronises on the
+ * recorded events and writes, per stage, the summed device milliseconds over the recorded
+ * calls into ms[LMOE_NUM_STAGES], the number of recorded calls into *calls and the number
+ * of kernels those calls launched into *launches (any output may be NULL). */
+#define LMOE_NUM_STAGES 8
+/* stage order: router GEMM, cutoff + top-K + segments, W_down GEMM, expert gate/up GEMM,
+ * expert down GEMM, RMSNorm + combine, shared gate/up GEMM, W_up + shared-down GEMM */
+LMOE_API lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable);
+LMOE_API lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t* launches);
+
+/* Library build identifier (static string): engine names per dtype. */
+LMOE_API const char* lmoe_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LMOE_H */

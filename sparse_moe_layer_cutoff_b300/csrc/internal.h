@@ -1,0 +1,86 @@
+// Internal launcher interfaces between the translation units of the library.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lmoe {
+
+constexpr int kMaxExperts = 4096;
+constexpr int kMaxTopK = 64;
+constexpr int kMaxShared = 3;
+constexpr int kSegTokens = 128;   // tokens per block of the segmentation kernels
+constexpr int kTileM = 128;       // rows per GEMM tile (m-tile prefix granularity)
+
+struct RouteArgs {
+  const float* logits;      // [bt, E]
+  const float* logits_t;    // [E, bt]
+  int bt, n_experts, top_k, tile_m;
+  double* alpha;            // [E]
+  int32_t* idx;             // [bt, K]
+  float* w;                 // [bt, K]
+  int32_t* block_cnt;       // [ceil(bt / kSegTokens), E]
+  int32_t* counts;          // [E]
+  int32_t* offsets;         // [E + 1]
+  int32_t* mtile_off;       // [E + 1]
+  int32_t* perm;            // [bt * K]
+  int32_t* inv;             // [bt * K]
+  int32_t* user_counts;     // optional [E]
+};
+
+constexpr int kRouteTailLaunches = 5;   // cutoff, top-K, count, scan, scatter
+cudaError_t route_tail_prepare();
+cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------------------- GEMMs
+// C[r, n] = sum_k A[arow(r), k] * B(g, n, k), with
+//   arow(r) = a_rows ? a_rows[r] : r            (row gather for the routed experts)
+//   B(g, n, k) = seg_B[s][(g * b_group_rows + n) * seg_ldb[s] + (k - seg_k0[s])]
+//               for the K segment s holding k    (K-concatenation of several weights)
+// Rows are grouped when seg_off != nullptr: group g owns rows [seg_off[g], seg_off[g+1])
+// and its m-tiles are numbered from mtile_off[g] (device arrays, set by the router).
+enum EpiKind { kEpiStore = 0, kEpiGlu = 1, kEpiRouter = 2 };
+// Which contraction of the layer a GemmArgs describes (the tensor-core engine keys its
+// prebuilt weight descriptors on it).
+enum GemmOp { kOpRouter = 0, kOpDown, kOpExpertGateUp, kOpExpertDown, kOpSharedGateUp, kOpFinal, kNumOps };
+
+constexpr int kMaxKSeg = 1 + kMaxShared;
+
+struct GemmArgs {
+  int M, N, K;                   // M: rows (dense), or the row capacity (grouped)
+  const void* A; long long lda;
+  const int32_t* a_rows;
+  int nseg;
+  int seg_k0[kMaxKSeg + 1];      // seg_k0[nseg] == K
+  const void* seg_B[kMaxKSeg];
+  long long seg_ldb[kMaxKSeg];
+  long long seg_row0[kMaxKSeg];  // extra B row offset per segment (e.g. shared expert j * d)
+  const void* B_up;              // GLU: up-branch weights, same layout as segment 0
+  long long b_group_rows;        // grouped: B rows per group (0 = same B for all groups)
+  const int32_t* seg_off;        // [G + 1] or nullptr
+  const int32_t* mtile_off;      // [G + 1] or nullptr
+  int G;
+  int max_mtiles;                // launch bound on m-tiles (grouped)
+  int epi;
+  void* out; long long ldo;      // Store / Glu: T; Router: fp32
+  float* out_t; long long ldt;   // Router: transposed logits [N, ldt]
+  const float* bias;             // Router: [N] or nullptr
+  float beta, beta_u;
+  int op;                        // GemmOp
+};
+
+cudaError_t launch_gemm_simt(const GemmArgs& a, bool is_bf16, cudaStream_t st);
+
+// ---------------------------------------------------------------------------- combine
+struct CombineArgs {
+  const void* y;          // [bt*K, L] slot-ordered expert outputs
+  const int32_t* inv;     // [bt, K]
+  const float* w;         // [bt, K]
+  const void* gamma;      // [L]
+  int bt, top_k, latent;
+  float eps;
+  void* cat; long long ldc;   // c written to cat[t, 0:L]
+};
+cudaError_t launch_combine(const CombineArgs& a, bool is_bf16, cudaStream_t st);
+
+}  // namespace lmoe

@@ -1,0 +1,478 @@
+// C ABI of the Stable LatentMoE layer forward: argument validation, the workspace, and the
+// launch sequence of the layer ("KimiK3的StableLatentMoE架构解析", ¶"具体前向流程" / Fig. 2:
+// router -> down_proj -> GroupedExperts -> latent_norm + weighted fusion -> up_proj, plus the
+// shared SiTU-GLU branch on the flattened input).
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/lmoe.h"
+#include "common.cuh"
+#include "gemm_tc.h"
+#include "internal.h"
+
+using namespace lmoe;
+
+struct lmoe_ctx {
+  lmoe_config cfg;
+  lmoe_weights w;
+  int max_bt;
+  int device;
+  int sm_count;
+  cudaStream_t stream;
+  bool bf16;
+  size_t esz;
+  bool check;
+  bool use_tc;
+  int last_bt;
+  // workspace (one allocation)
+  char* ws;
+  size_t ws_bytes;
+  float* logits;
+  float* logits_t;
+  double* alpha;
+  int32_t* idx;
+  float* wk;
+  int32_t* block_cnt;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* mtile_off;
+  int32_t* perm;
+  int32_t* inv;
+  void* z;
+  void* h;
+  void* y;
+  void* cat;
+  uint32_t* status;
+  TcPlan* tc;
+  // per-stage profiling
+  bool prof_on;
+  int prof_calls;
+  std::vector<cudaEvent_t> prof_ev;   // [kProfCap][LMOE_NUM_STAGES + 1]
+  long long launches;
+  long long prof_launch_base;
+};
+
+namespace {
+
+constexpr int kProfCap = 1024;
+
+void prof_mark(lmoe_ctx* ctx, int boundary, cudaStream_t st) {
+  if (!ctx->prof_on || ctx->prof_calls >= kProfCap) return;
+  cudaEventRecord(ctx->prof_ev[(size_t)ctx->prof_calls * (LMOE_NUM_STAGES + 1) + boundary], st);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lmoe_status check_cfg(const lmoe_config* c) {
+  if (!c) return LMOE_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->latent <= 0 || c->n_experts <= 0 || c->top_k <= 0 || c->expert_inter <= 0 ||
+      c->n_shared <= 0 || c->shared_inter <= 0)
+    return LMOE_ERR_INVALID_ARG;
+  if (c->top_k > c->n_experts) return LMOE_ERR_INVALID_ARG;
+  if (c->dtype != LMOE_F32 && c->dtype != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
+  if (!(c->beta > 0.f) || !(c->beta_u > 0.f) || !(c->rms_eps >= 0.f) || c->beta > 3.0e38f ||
+      c->beta_u > 3.0e38f || c->rms_eps > 3.0e38f)
+    return LMOE_ERR_INVALID_ARG;
+  if (c->n_experts > kMaxExperts || c->top_k > kMaxTopK || c->n_shared > kMaxShared)
+    return LMOE_ERR_UNSUPPORTED;
+  if (c->dtype == LMOE_BF16) {
+    if (c->d % 64 || c->latent % 64 || c->expert_inter % 64 || c->shared_inter % 64)
+      return LMOE_ERR_UNSUPPORTED;
+  } else {
+    if (c->latent % 4 || c->shared_inter % 4) return LMOE_ERR_UNSUPPORTED;
+  }
+  // int32 element offsets inside one weight matrix / row must not overflow
+  const long long big = (long long)c->n_experts * c->expert_inter * c->latent;
+  if (big >= (1LL << 40)) return LMOE_ERR_UNSUPPORTED;
+  return LMOE_OK;
+}
+
+lmoe_status check_device_ptr(const void* p) {
+  if (!p) return LMOE_ERR_INVALID_ARG;
+  if (!aligned16(p)) return LMOE_ERR_INVALID_ARG;
+  cudaPointerAttributes at;
+  cudaError_t e = cudaPointerGetAttributes(&at, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_INVALID_ARG;
+  }
+  if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return LMOE_ERR_INVALID_ARG;
+  return LMOE_OK;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Carve {
+  size_t off = 0;
+  template <typename T>
+  size_t take(size_t count) {
+    size_t o = off;
+    off = align_up(off + count * sizeof(T), 256);
+    return o;
+  }
+};
+
+lmoe_status finish(lmoe_ctx* ctx, cudaStream_t st, cudaError_t e) {
+  if (e != cudaSuccess) return LMOE_ERR_CUDA;
+  if (ctx->check) return lmoe_sync_status(ctx, st);
+  return LMOE_OK;
+}
+
+cudaError_t run_gemm(lmoe_ctx* ctx, const GemmArgs& g, cudaStream_t st) {
+  ctx->launches += 1;
+  if (ctx->use_tc) return launch_gemm_tc(ctx->tc, g, st);
+  return launch_gemm_simt(g, ctx->bf16, st);
+}
+
+GemmArgs base_args(const lmoe_ctx* ctx) {
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.nseg = 1;
+  g.beta = ctx->cfg.beta;
+  g.beta_u = ctx->cfg.beta_u;
+  return g;
+}
+
+cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, int32_t* user_counts) {
+  const lmoe_config& c = ctx->cfg;
+  GemmArgs g = base_args(ctx);
+  g.M = bt; g.N = c.n_experts; g.K = c.d;
+  g.A = x; g.lda = c.d;
+  g.seg_k0[0] = 0; g.seg_k0[1] = c.d;
+  g.seg_B[0] = ctx->w.w_router; g.seg_ldb[0] = c.d;
+  g.epi = kEpiRouter;
+  g.out = ctx->logits; g.ldo = c.n_experts;
+  g.out_t = ctx->logits_t; g.ldt = bt;
+  g.bias = ctx->w.router_bias;
+  g.op = kOpRouter;
+  cudaError_t e = run_gemm(ctx, g, st);
+  if (e != cudaSuccess) return e;
+  prof_mark(ctx, 1, st);
+  RouteArgs r;
+  r.logits = ctx->logits; r.logits_t = ctx->logits_t;
+  r.bt = bt; r.n_experts = c.n_experts; r.top_k = c.top_k; r.tile_m = kTileM;
+  r.alpha = ctx->alpha; r.idx = ctx->idx; r.w = ctx->wk;
+  r.block_cnt = ctx->block_cnt; r.counts = ctx->counts; r.offsets = ctx->offsets;
+  r.mtile_off = ctx->mtile_off; r.perm = ctx->perm; r.inv = ctx->inv;
+  r.user_counts = user_counts;
+  ctx->launches += kRouteTailLaunches;
+  return launch_route_tail(r, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* lmoe_status_string(lmoe_status s) {
+  switch (s) {
+    case LMOE_OK: return "LMOE_OK";
+    case LMOE_ERR_INVALID_ARG: return "LMOE_ERR_INVALID_ARG";
+    case LMOE_ERR_UNSUPPORTED: return "LMOE_ERR_UNSUPPORTED";
+    case LMOE_ERR_OOM: return "LMOE_ERR_OOM";
+    case LMOE_ERR_CUDA: return "LMOE_ERR_CUDA";
+    case LMOE_ERR_TIMEOUT: return "LMOE_ERR_TIMEOUT";
+    case LMOE_ERR_DEVICE_ASSERT: return "LMOE_ERR_DEVICE_ASSERT";
+  }
+  return "LMOE_ERR_UNKNOWN";
+}
+
+const char* lmoe_build_info(void) {
+  return "lmoe sm_103a: bf16 = tcgen05/TMEM/TMA GEMMs, fp32 = CUDA-core fp32 FMA GEMMs";
+}
+
+lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt,
+                        lmoe_stream stream, lmoe_ctx** out) {
+  if (!out) return LMOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  lmoe_status s = check_cfg(cfg);
+  if (s != LMOE_OK) return s;
+  if (!w) return LMOE_ERR_INVALID_ARG;
+  if (max_bt <= 0 || max_bt > (1 << 20)) return LMOE_ERR_INVALID_ARG;
+  if ((long long)max_bt * cfg->top_k >= (1LL << 31)) return LMOE_ERR_UNSUPPORTED;
+  const void* req[] = {w->w_router, w->w_down, w->latent_gamma, w->w_up, w->exp_gate,
+                       w->exp_up, w->exp_down, w->sh_gate, w->sh_up, w->sh_down};
+  for (const void* p : req)
+    if (!p || !aligned16(p)) return LMOE_ERR_INVALID_ARG;
+  if (w->router_bias && !aligned16(w->router_bias)) return LMOE_ERR_INVALID_ARG;
+  // from here on the CUDA runtime is needed
+  for (const void* p : req)
+    if ((s = check_device_ptr(p)) != LMOE_OK) return s;
+  if (w->router_bias && (s = check_device_ptr(w->router_bias)) != LMOE_OK) return s;
+
+  lmoe_ctx* ctx = new (std::nothrow) lmoe_ctx();
+  if (!ctx) return LMOE_ERR_OOM;
+  ctx->cfg = *cfg;
+  ctx->w = *w;
+  ctx->max_bt = max_bt;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  ctx->bf16 = cfg->dtype == LMOE_BF16;
+  ctx->esz = ctx->bf16 ? 2 : 4;
+  const char* chk = getenv("LMOE_CHECK");
+  ctx->check = chk && chk[0] == '1';
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess ||
+      route_tail_prepare() != cudaSuccess) {
+    cudaGetLastError();
+    delete ctx;
+    return LMOE_ERR_CUDA;
+  }
+
+  const lmoe_config& c = *cfg;
+  const size_t bt = (size_t)max_bt, E = c.n_experts, K = c.top_k, L = c.latent;
+  const size_t nblk = (bt + kSegTokens - 1) / kSegTokens;
+  const size_t ldc = L + (size_t)c.n_shared * c.shared_inter;
+  Carve cv;
+  size_t o_logits = cv.take<float>(bt * E);
+  size_t o_logits_t = cv.take<float>(bt * E);
+  size_t o_alpha = cv.take<double>(E);
+  size_t o_idx = cv.take<int32_t>(bt * K);
+  size_t o_w = cv.take<float>(bt * K);
+  size_t o_bcnt = cv.take<int32_t>(nblk * E);
+  size_t o_cnt = cv.take<int32_t>(E);
+  size_t o_off = cv.take<int32_t>(E + 1);
+  size_t o_mt = cv.take<int32_t>(E + 1);
+  size_t o_perm = cv.take<int32_t>(bt * K);
+  size_t o_inv = cv.take<int32_t>(bt * K);
+  size_t o_status = cv.take<uint32_t>(4);
+  size_t o_z = cv.take<char>(bt * L * ctx->esz);
+  size_t o_h = cv.take<char>(bt * K * c.expert_inter * ctx->esz);
+  size_t o_y = cv.take<char>(bt * K * L * ctx->esz);
+  size_t o_cat = cv.take<char>(bt * ldc * ctx->esz);
+  ctx->ws_bytes = cv.off;
+  if (cudaMalloc(&ctx->ws, ctx->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete ctx;
+    return LMOE_ERR_OOM;
+  }
+  char* b = ctx->ws;
+  ctx->logits = (float*)(b + o_logits);
+  ctx->logits_t = (float*)(b + o_logits_t);
+  ctx->alpha = (double*)(b + o_alpha);
+  ctx->idx = (int32_t*)(b + o_idx);
+  ctx->wk = (float*)(b + o_w);
+  ctx->block_cnt = (int32_t*)(b + o_bcnt);
+  ctx->counts = (int32_t*)(b + o_cnt);
+  ctx->offsets = (int32_t*)(b + o_off);
+  ctx->mtile_off = (int32_t*)(b + o_mt);
+  ctx->perm = (int32_t*)(b + o_perm);
+  ctx->inv = (int32_t*)(b + o_inv);
+  ctx->status = (uint32_t*)(b + o_status);
+  ctx->z = b + o_z;
+  ctx->h = b + o_h;
+  ctx->y = b + o_y;
+  ctx->cat = b + o_cat;
+  if (cudaMemset(ctx->ws, 0, ctx->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(ctx->ws);
+    delete ctx;
+    return LMOE_ERR_CUDA;
+  }
+  ctx->use_tc = false;
+  ctx->tc = nullptr;
+  if (ctx->bf16) {
+    const char* force = getenv("LMOE_FORCE_SIMT");
+    if (!(force && force[0] == '1')) {
+      TcBuffers tb;
+      tb.z = ctx->z; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
+      tb.status = ctx->status;
+      lmoe_status ts = tc_plan_create(&c, w, max_bt, ctx->sm_count, tb, &ctx->tc);
+      if (ts != LMOE_OK) {
+        cudaFree(ctx->ws);
+        delete ctx;
+        return ts;
+      }
+      ctx->use_tc = ctx->tc != nullptr;
+    }
+  }
+  *out = ctx;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream,
+                       int32_t* topk_idx, float* topk_w, int32_t* expert_counts, double* alpha,
+                       float* logits) {
+  if (!ctx || bt < 0 || bt > ctx->max_bt) return LMOE_ERR_INVALID_ARG;
+  if (bt == 0) return LMOE_OK;
+  if (!x || !aligned16(x)) return LMOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const lmoe_config& c = ctx->cfg;
+  ctx->last_bt = bt;
+  cudaError_t e = route_impl(ctx, x, bt, st, expert_counts);
+  const size_t btK = (size_t)bt * c.top_k;
+  if (e == cudaSuccess && topk_idx)
+    e = cudaMemcpyAsync(topk_idx, ctx->idx, btK * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && topk_w)
+    e = cudaMemcpyAsync(topk_w, ctx->wk, btK * 4, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && alpha)
+    e = cudaMemcpyAsync(alpha, ctx->alpha, (size_t)c.n_experts * 8, cudaMemcpyDeviceToDevice, st);
+  if (e == cudaSuccess && logits)
+    e = cudaMemcpyAsync(logits, ctx->logits, (size_t)bt * c.n_experts * 4, cudaMemcpyDeviceToDevice, st);
+  return finish(ctx, st, e);
+}
+
+lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream) {
+  if (!ctx || bt < 0 || bt > ctx->max_bt) return LMOE_ERR_INVALID_ARG;
+  if (bt == 0) return LMOE_OK;
+  if (!x || !out || !aligned16(x) || !aligned16(out)) return LMOE_ERR_INVALID_ARG;
+  const lmoe_config& c = ctx->cfg;
+  const size_t xbytes = (size_t)bt * c.d * ctx->esz;
+  const char* xb = static_cast<const char*>(x);
+  const char* ob = static_cast<const char*>(out);
+  if (ob < xb + xbytes && xb < ob + xbytes) return LMOE_ERR_INVALID_ARG;  // out overlaps x
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  ctx->last_bt = bt;
+  prof_mark(ctx, 0, st);
+  cudaError_t e = route_impl(ctx, x, bt, st, nullptr);
+  prof_mark(ctx, 2, st);
+  const long long ldc = (long long)c.latent + (long long)c.n_shared * c.shared_inter;
+  const int max_mtiles = (int)(((long long)bt * c.top_k) / kTileM + c.n_experts + 1);
+
+  if (e == cudaSuccess) {  // z = x W_down^T
+    GemmArgs g = base_args(ctx);
+    g.M = bt; g.N = c.latent; g.K = c.d;
+    g.A = x; g.lda = c.d;
+    g.seg_k0[1] = c.d; g.seg_B[0] = ctx->w.w_down; g.seg_ldb[0] = c.d;
+    g.epi = kEpiStore; g.out = ctx->z; g.ldo = c.latent;
+    g.op = kOpDown;
+    e = run_gemm(ctx, g, st);
+    prof_mark(ctx, 3, st);
+  }
+  if (e == cudaSuccess) {  // h[slot] = act(W_g[e] z[perm[slot]], W_u[e] z[perm[slot]])
+    GemmArgs g = base_args(ctx);
+    g.M = bt * c.top_k; g.N = c.expert_inter; g.K = c.latent;
+    g.A = ctx->z; g.lda = c.latent; g.a_rows = ctx->perm;
+    g.seg_k0[1] = c.latent; g.seg_B[0] = ctx->w.exp_gate; g.seg_ldb[0] = c.latent;
+    g.B_up = ctx->w.exp_up; g.b_group_rows = c.expert_inter;
+    g.seg_off = ctx->offsets; g.mtile_off = ctx->mtile_off; g.G = c.n_experts; g.max_mtiles = max_mtiles;
+    g.epi = kEpiGlu; g.out = ctx->h; g.ldo = c.expert_inter;
+    g.op = kOpExpertGateUp;
+    e = run_gemm(ctx, g, st);
+    prof_mark(ctx, 4, st);
+  }
+  if (e == cudaSuccess) {  // y[slot] = W_d[e] h[slot]
+    GemmArgs g = base_args(ctx);
+    g.M = bt * c.top_k; g.N = c.latent; g.K = c.expert_inter;
+    g.A = ctx->h; g.lda = c.expert_inter;
+    g.seg_k0[1] = c.expert_inter; g.seg_B[0] = ctx->w.exp_down; g.seg_ldb[0] = c.expert_inter;
+    g.b_group_rows = c.latent;
+    g.seg_off = ctx->offsets; g.mtile_off = ctx->mtile_off; g.G = c.n_experts; g.max_mtiles = max_mtiles;
+    g.epi = kEpiStore; g.out = ctx->y; g.ldo = c.latent;
+    g.op = kOpExpertDown;
+    e = run_gemm(ctx, g, st);
+    prof_mark(ctx, 5, st);
+  }
+  if (e == cudaSuccess) {  // c = sum_k w RMSNorm(y_k) -> cat[:, 0:L]
+    CombineArgs a;
+    a.y = ctx->y; a.inv = ctx->inv; a.w = ctx->wk; a.gamma = ctx->w.latent_gamma;
+    a.bt = bt; a.top_k = c.top_k; a.latent = c.latent; a.eps = c.rms_eps;
+    a.cat = ctx->cat; a.ldc = ldc;
+    e = launch_combine(a, ctx->bf16, st);
+    ctx->launches += 1;
+    prof_mark(ctx, 6, st);
+  }
+  if (e == cudaSuccess) {  // shared activations -> cat[:, L:]
+    GemmArgs g = base_args(ctx);
+    g.M = bt; g.N = c.n_shared * c.shared_inter; g.K = c.d;
+    g.A = x; g.lda = c.d;
+    g.seg_k0[1] = c.d; g.seg_B[0] = ctx->w.sh_gate; g.seg_ldb[0] = c.d;
+    g.B_up = ctx->w.sh_up;
+    g.epi = kEpiGlu;
+    g.out = static_cast<char*>(ctx->cat) + (size_t)c.latent * ctx->esz; g.ldo = ldc;
+    g.op = kOpSharedGateUp;
+    e = run_gemm(ctx, g, st);
+    prof_mark(ctx, 7, st);
+  }
+  if (e == cudaSuccess) {  // out = [c | h_sh] [W_up | W_d^sh_0 | ...]^T
+    GemmArgs g = base_args(ctx);
+    g.M = bt; g.N = c.d; g.K = (int)ldc;
+    g.A = ctx->cat; g.lda = ldc;
+    g.nseg = 1 + c.n_shared;
+    g.seg_k0[0] = 0; g.seg_B[0] = ctx->w.w_up; g.seg_ldb[0] = c.latent; g.seg_row0[0] = 0;
+    for (int j = 0; j < c.n_shared; ++j) {
+      g.seg_k0[1 + j] = c.latent + j * c.shared_inter;
+      g.seg_B[1 + j] = ctx->w.sh_down;
+      g.seg_ldb[1 + j] = c.shared_inter;
+      g.seg_row0[1 + j] = (long long)j * c.d;
+    }
+    g.seg_k0[g.nseg] = (int)ldc;
+    g.epi = kEpiStore; g.out = out; g.ldo = c.d;
+    g.op = kOpFinal;
+    e = run_gemm(ctx, g, st);
+    prof_mark(ctx, 8, st);
+  }
+  if (ctx->prof_on && ctx->prof_calls < kProfCap) ctx->prof_calls++;
+  return finish(ctx, st, e);
+}
+
+lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable) {
+  if (!ctx) return LMOE_ERR_INVALID_ARG;
+  if (enable && ctx->prof_ev.empty()) {
+    ctx->prof_ev.resize((size_t)kProfCap * (LMOE_NUM_STAGES + 1));
+    for (auto& ev : ctx->prof_ev)
+      if (cudaEventCreate(&ev) != cudaSuccess) return LMOE_ERR_CUDA;
+  }
+  if (enable) { ctx->prof_calls = 0; ctx->prof_launch_base = ctx->launches; }
+  ctx->prof_on = enable != 0;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t* launches) {
+  if (!ctx) return LMOE_ERR_INVALID_ARG;
+  float acc[LMOE_NUM_STAGES] = {0};
+  for (int c = 0; c < ctx->prof_calls; ++c) {
+    cudaEvent_t* ev = &ctx->prof_ev[(size_t)c * (LMOE_NUM_STAGES + 1)];
+    if (cudaEventSynchronize(ev[LMOE_NUM_STAGES]) != cudaSuccess) return LMOE_ERR_CUDA;
+    for (int s = 0; s < LMOE_NUM_STAGES; ++s) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return LMOE_ERR_CUDA;
+      acc[s] += t;
+    }
+  }
+  if (ms) for (int s = 0; s < LMOE_NUM_STAGES; ++s) ms[s] = acc[s];
+  if (calls) *calls = ctx->prof_calls;
+  if (launches) *launches = ctx->launches - ctx->prof_launch_base;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream) {
+  if (!ctx) return LMOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LMOE_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, ctx->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (v && cudaMemset(ctx->status, 0, 4) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (v & kStatusTimeout) return LMOE_ERR_TIMEOUT;
+  if (v & kStatusAssert) return LMOE_ERR_DEVICE_ASSERT;
+  return LMOE_OK;
+}
+
+void lmoe_destroy(lmoe_ctx* ctx) {
+  if (!ctx) return;
+  cudaDeviceSynchronize();
+  for (auto& ev : ctx->prof_ev) cudaEventDestroy(ev);
+  tc_plan_destroy(ctx->tc);
+  cudaFree(ctx->ws);
+  delete ctx;
+}
+
+lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* v) {
+  if (!ctx || !v) return LMOE_ERR_INVALID_ARG;
+  v->bt = ctx->last_bt;
+  v->logits = ctx->logits;
+  v->alpha = ctx->alpha;
+  v->topk_idx = ctx->idx;
+  v->topk_w = ctx->wk;
+  v->offsets = ctx->offsets;
+  v->perm = ctx->perm;
+  v->inv = ctx->inv;
+  v->z = ctx->z;
+  v->h = ctx->h;
+  v->y = ctx->y;
+  v->cat = ctx->cat;
+  return LMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,274 @@
+"""Python binding of liblmoe.so (ctypes).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA kernels.
+The low-level functions carry the C names (lmoe_create, lmoe_route, lmoe_forward,
+lmoe_destroy, ...) and take raw integers for device pointers and streams.
+`LatentMoE` wraps them for torch tensors: it keeps the borrowed weights alive and
+allocates output tensors with torch (device memory and streams are torch's; no
+arithmetic is done in Python).  There is no fallback: if the library is missing the
+import of a function raises."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "liblmoe.so")
+HEADER = os.path.join(os.path.dirname(PKG), "include", "lmoe.h")
+
+LMOE_OK, LMOE_ERR_INVALID_ARG, LMOE_ERR_UNSUPPORTED, LMOE_ERR_OOM, LMOE_ERR_CUDA, \
+    LMOE_ERR_TIMEOUT, LMOE_ERR_DEVICE_ASSERT = range(7)
+LMOE_F32, LMOE_BF16 = 0, 1
+
+c_i32, c_f32, c_vp = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+
+
+class lmoe_config(ctypes.Structure):
+    _fields_ = [("d", c_i32), ("latent", c_i32), ("n_experts", c_i32), ("top_k", c_i32),
+                ("expert_inter", c_i32), ("n_shared", c_i32), ("shared_inter", c_i32),
+                ("beta", c_f32), ("beta_u", c_f32), ("rms_eps", c_f32), ("dtype", c_i32)]
+
+
+class lmoe_weights(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("w_router", "router_bias", "w_down", "latent_gamma", "w_up",
+                                    "exp_gate", "exp_up", "exp_down", "sh_gate", "sh_up", "sh_down")]
+
+
+class lmoe_workspace_view(ctypes.Structure):
+    _fields_ = [("bt", c_i32)] + [(n, c_vp) for n in ("logits", "alpha", "topk_idx", "topk_w", "offsets",
+                                                       "perm", "inv", "z", "h", "y", "cat")]
+
+
+class LmoeError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {lmoe_status_string(status)}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load liblmoe.so (built in-tree by `python -m sparse_moe_layer_cutoff_b300.build`)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m sparse_moe_layer_cutoff_b300.build`")
+    lib = ctypes.CDLL(path)
+    lib.lmoe_create.argtypes = [ctypes.POINTER(lmoe_config), ctypes.POINTER(lmoe_weights), c_i32, c_vp,
+                                ctypes.POINTER(c_vp)]
+    lib.lmoe_create.restype = c_i32
+    lib.lmoe_route.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp]
+    lib.lmoe_route.restype = c_i32
+    lib.lmoe_forward.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
+    lib.lmoe_forward.restype = c_i32
+    lib.lmoe_sync_status.argtypes = [c_vp, c_vp]
+    lib.lmoe_sync_status.restype = c_i32
+    lib.lmoe_destroy.argtypes = [c_vp]
+    lib.lmoe_destroy.restype = None
+    lib.lmoe_status_string.argtypes = [c_i32]
+    lib.lmoe_status_string.restype = ctypes.c_char_p
+    lib.lmoe_workspace.argtypes = [c_vp, ctypes.POINTER(lmoe_workspace_view)]
+    lib.lmoe_workspace.restype = c_i32
+    lib.lmoe_profile.argtypes = [c_vp, c_i32]
+    lib.lmoe_profile.restype = c_i32
+    lib.lmoe_profile_read.argtypes = [c_vp, ctypes.POINTER(c_f32), ctypes.POINTER(c_i32),
+                                      ctypes.POINTER(ctypes.c_int64)]
+    lib.lmoe_profile_read.restype = c_i32
+    lib.lmoe_build_info.argtypes = []
+    lib.lmoe_build_info.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def declared_symbols(header: str = HEADER) -> list[str]:
+    """Names of the functions include/lmoe.h declares."""
+    text = open(header).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lmoe_[a-z_]+)\s*\(", text)))
+
+
+# ----------------------------------------------------------------------------- C names
+
+def lmoe_status_string(status: int) -> str:
+    return load_library().lmoe_status_string(status).decode()
+
+
+def lmoe_create(cfg: lmoe_config, weights: lmoe_weights, max_bt: int, stream: int = 0):
+    """Returns (status, ctx handle or None)."""
+    out = c_vp()
+    st = load_library().lmoe_create(ctypes.byref(cfg), ctypes.byref(weights), max_bt, c_vp(stream),
+                                    ctypes.byref(out))
+    return st, (out.value if st == LMOE_OK else None)
+
+
+def lmoe_route(ctx, x: int, bt: int, stream: int = 0, topk_idx: int = 0, topk_w: int = 0,
+               expert_counts: int = 0, alpha: int = 0, logits: int = 0) -> int:
+    return load_library().lmoe_route(c_vp(ctx), c_vp(x), bt, c_vp(stream), c_vp(topk_idx), c_vp(topk_w),
+                                     c_vp(expert_counts), c_vp(alpha), c_vp(logits))
+
+
+def lmoe_forward(ctx, x: int, bt: int, out: int, stream: int = 0) -> int:
+    return load_library().lmoe_forward(c_vp(ctx), c_vp(x), bt, c_vp(out), c_vp(stream))
+
+
+def lmoe_sync_status(ctx, stream: int = 0) -> int:
+    return load_library().lmoe_sync_status(c_vp(ctx), c_vp(stream))
+
+
+def lmoe_destroy(ctx) -> None:
+    load_library().lmoe_destroy(c_vp(ctx))
+
+
+def lmoe_workspace(ctx) -> lmoe_workspace_view:
+    v = lmoe_workspace_view()
+    st = load_library().lmoe_workspace(c_vp(ctx), ctypes.byref(v))
+    if st != LMOE_OK:
+        raise LmoeError(st, "lmoe_workspace")
+    return v
+
+
+LMOE_NUM_STAGES = 8
+STAGE_NAMES = ("router_gemm", "cutoff_topk_segments", "w_down_gemm", "expert_gate_up_gemm",
+               "expert_down_gemm", "rmsnorm_combine", "shared_gate_up_gemm", "up_shared_down_gemm")
+
+
+def lmoe_profile(ctx, enable: bool) -> int:
+    return load_library().lmoe_profile(c_vp(ctx), 1 if enable else 0)
+
+
+def lmoe_profile_read(ctx):
+    """Returns (status, {stage: summed ms}, recorded calls, kernels launched)."""
+    ms = (c_f32 * LMOE_NUM_STAGES)()
+    calls, launches = c_i32(), ctypes.c_int64()
+    st = load_library().lmoe_profile_read(c_vp(ctx), ms, ctypes.byref(calls), ctypes.byref(launches))
+    return st, dict(zip(STAGE_NAMES, list(ms))), calls.value, launches.value
+
+
+def lmoe_build_info() -> str:
+    return load_library().lmoe_build_info().decode()
+
+
+# ----------------------------------------------------------------------------- torch wrapper
+
+def make_config(shape) -> lmoe_config:
+    """From any object with the lmoe_config field names (dtype "bf16" / "f32")."""
+    return lmoe_config(shape.d, shape.latent, shape.n_experts, shape.top_k, shape.expert_inter,
+                       shape.n_shared, shape.shared_inter, shape.beta, shape.beta_u, shape.rms_eps,
+                       LMOE_BF16 if shape.dtype == "bf16" else LMOE_F32)
+
+
+WEIGHT_NAMES = ("w_router", "w_down", "latent_gamma", "w_up", "exp_gate", "exp_up", "exp_down",
+                "sh_gate", "sh_up", "sh_down")
+
+
+class LatentMoE:
+    """One layer context over borrowed torch CUDA tensors."""
+
+    def __init__(self, shape, weights: dict, max_bt: int, router_bias=None, stream=None):
+        import torch
+
+        self.shape = shape
+        self.dtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+        self._keep = dict(weights)
+        self._bias = router_bias
+        w = lmoe_weights()
+        for n in WEIGHT_NAMES:
+            t = weights[n]
+            if not t.is_contiguous():
+                raise ValueError(f"{n} must be contiguous")
+            setattr(w, n, t.data_ptr())
+        w.router_bias = router_bias.data_ptr() if router_bias is not None else None
+        self.cfg = make_config(shape)
+        self.max_bt = max_bt
+        s = torch.cuda.current_stream() if stream is None else stream
+        st, ctx = lmoe_create(self.cfg, w, max_bt, s.cuda_stream)
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_create")
+        self.ctx = ctx
+
+    def _stream(self, stream):
+        import torch
+        return (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+
+    def route(self, x, stream=None) -> dict:
+        import torch
+        bt = x.shape[0]
+        s = self.shape
+        dev = x.device
+        out = dict(idx=torch.empty((bt, s.top_k), dtype=torch.int32, device=dev),
+                   w=torch.empty((bt, s.top_k), dtype=torch.float32, device=dev),
+                   counts=torch.empty((s.n_experts,), dtype=torch.int32, device=dev),
+                   alpha=torch.empty((s.n_experts,), dtype=torch.float64, device=dev),
+                   logits=torch.empty((bt, s.n_experts), dtype=torch.float32, device=dev))
+        st = lmoe_route(self.ctx, x.data_ptr(), bt, self._stream(stream), out["idx"].data_ptr(),
+                        out["w"].data_ptr(), out["counts"].data_ptr(), out["alpha"].data_ptr(),
+                        out["logits"].data_ptr())
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_route")
+        return out
+
+    def forward(self, x, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty((x.shape[0], self.shape.d), dtype=self.dtype, device=x.device)
+        st = lmoe_forward(self.ctx, x.data_ptr(), x.shape[0], out.data_ptr(), self._stream(stream))
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_forward")
+        return out
+
+    def sync_status(self, stream=None) -> int:
+        return lmoe_sync_status(self.ctx, self._stream(stream))
+
+    def workspace(self) -> lmoe_workspace_view:
+        return lmoe_workspace(self.ctx)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lmoe_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class _DevArray:
+    """Zero-copy view of a device buffer for torch.as_tensor (CUDA array interface)."""
+
+    def __init__(self, ptr: int, shape: tuple, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (ptr, False),
+                                         "version": 2, "strides": None}
+
+
+def workspace_tensors(layer: "LatentMoE") -> dict:
+    """torch views (no copy) of the intermediates of the layer's last call."""
+    import torch
+
+    v = layer.workspace()
+    s, bt = layer.shape, v.bt
+    el = "<i2" if s.dtype == "bf16" else "<f4"
+
+    def view(ptr, shape, typestr, dtype=None):
+        t = torch.as_tensor(_DevArray(ptr, shape, typestr), device="cuda")
+        return t.view(dtype) if dtype is not None else t
+
+    fdt = torch.bfloat16 if s.dtype == "bf16" else None
+    ldc = s.latent + s.n_shared * s.shared_inter
+    return dict(
+        logits=view(v.logits, (bt, s.n_experts), "<f4"),
+        alpha=view(v.alpha, (s.n_experts,), "<f8"),
+        idx=view(v.topk_idx, (bt, s.top_k), "<i4"),
+        w=view(v.topk_w, (bt, s.top_k), "<f4"),
+        offsets=view(v.offsets, (s.n_experts + 1,), "<i4"),
+        perm=view(v.perm, (bt * s.top_k,), "<i4"),
+        inv=view(v.inv, (bt, s.top_k), "<i4"),
+        z=view(v.z, (bt, s.latent), el, fdt),
+        h=view(v.h, (bt * s.top_k, s.expert_inter), el, fdt),
+        y=view(v.y, (bt * s.top_k, s.latent), el, fdt),
+        cat=view(v.cat, (bt, ldc), el, fdt),
+    )

@@ -1,0 +1,117 @@
+"""Glue for the GPU parity tests: run the CUDA library on seeded inputs and compare it
+with the fp64 oracle.  Inputs come from workloads.py only; expected values come from
+the oracle only."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import lmoe_oracle as O
+from sparse_moe_layer_cutoff_b300 import LatentMoE
+from sparse_moe_layer_cutoff_b300.lmoe import workspace_tensors
+from workloads import make_inputs
+
+BF16_MAX_ABS, BF16_REL_L2 = 2e-2, 1e-2       # output tolerance, bf16 layers
+F32_REL_L2 = 1e-5                            # output tolerance, fp32 layer
+W_RTOL, ALPHA_RTOL = 1e-6, 1e-15             # combine weights (fp32 storage), cutoffs (fp64)
+GAP_MIN = 1e-12                              # key margin that makes fp64 selections comparable
+
+
+def to64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().to(torch.float64).numpy()
+
+
+class PerIndex:
+    """Indexable provider of fp64 slices of a (device) tensor, fetched on demand."""
+
+    def __init__(self, t: torch.Tensor):
+        self.t = t
+
+    def __getitem__(self, i):
+        return to64(self.t[int(i)])
+
+    def __len__(self):
+        return self.t.shape[0]
+
+
+def oracle_weights(weights: dict) -> dict:
+    W = {}
+    for k, v in weights.items():
+        if k in ("exp_gate", "exp_up", "exp_down", "sh_gate", "sh_up", "sh_down"):
+            W[k] = PerIndex(v)
+        else:
+            W[k] = to64(v)
+    return W
+
+
+def rel_l2(a: np.ndarray, b: np.ndarray) -> float:
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
+
+
+class Run:
+    """One forward of the CUDA layer on a workload, with everything needed to check it."""
+
+    def __init__(self, workload, bt=None, x=None, weights=None, bias=None, max_bt=None):
+        if x is None:
+            x, weights, bias = make_inputs(workload, "cuda", bt)
+        self.w = workload
+        self.shape = workload.shape
+        self.x, self.weights, self.bias = x, weights, bias
+        self.bt = x.shape[0]
+        self.layer = LatentMoE(self.shape, weights, max_bt=max_bt or max(self.bt, 1), router_bias=bias)
+        self.route = self.layer.route(x)
+        self.out = self.layer.forward(x)
+        torch.cuda.synchronize()
+        self.status = self.layer.sync_status()
+        self.ws = workspace_tensors(self.layer)
+
+    def close(self):
+        self.layer.close()
+
+    # ------------------------------------------------------------------ routing parity
+    def check_routing(self):
+        K = self.shape.top_k
+        logits = self.route["logits"]
+        ref = O.route(to64(logits), K)
+        assert ref["min_gap"] > GAP_MIN, f"keys too close to compare selections: {ref['min_gap']}"
+        np.testing.assert_array_equal(self.route["idx"].cpu().numpy(), ref["idx"])
+        np.testing.assert_array_equal(self.route["counts"].cpu().numpy(), ref["counts"])
+        np.testing.assert_allclose(self.route["alpha"].cpu().numpy(), ref["alpha"], rtol=ALPHA_RTOL, atol=0)
+        np.testing.assert_allclose(to64(self.route["w"]), ref["w"], rtol=W_RTOL, atol=0)
+        # the forward's own routing (workspace) equals the route call's
+        np.testing.assert_array_equal(self.ws["idx"].cpu().numpy(), ref["idx"])
+        np.testing.assert_array_equal(self.ws["offsets"].cpu().numpy(), ref["offsets"])
+        np.testing.assert_array_equal(self.ws["perm"].cpu().numpy(), ref["perm"])
+        np.testing.assert_array_equal(self.ws["inv"].cpu().numpy(), ref["inv"])
+        return ref
+
+    def check_logits(self, rows=None, rtol=2e-3):
+        """The router GEMM against fp64 x W_r^T (+ b) on the given rows."""
+        rows = np.arange(self.bt) if rows is None else np.asarray(rows)
+        ref = O.router_logits(to64(self.x[rows]), to64(self.weights["w_router"]),
+                              None if self.bias is None else to64(self.bias))
+        got = to64(self.route["logits"][rows])
+        err = np.abs(got - ref).max()
+        scale = np.abs(ref).max() + 1e-30
+        assert err <= rtol * scale, (err, scale)
+
+    # ------------------------------------------------------------------ output parity
+    def oracle_out(self, rows, ref_route):
+        rows = np.asarray(rows)
+        s = self.shape
+        return O.layer_forward(to64(self.x[rows]), ref_route["idx"][rows], ref_route["w"][rows],
+                               oracle_weights(self.weights), s.beta, s.beta_u, s.rms_eps)
+
+    def check_output(self, rows=None, ref_route=None):
+        rows = np.arange(self.bt) if rows is None else np.asarray(rows)
+        ref_route = ref_route or self.check_routing()
+        ref = self.oracle_out(rows, ref_route)
+        got = to64(self.out[rows])
+        r = rel_l2(got, ref)
+        m = float(np.abs(got - ref).max())
+        if self.shape.dtype == "f32":
+            assert r <= F32_REL_L2, (r, m)
+        else:
+            assert m <= BF16_MAX_ABS and r <= BF16_REL_L2, (m, r)
+        return m, r

@@ -1,0 +1,91 @@
+"""The C-ABI library: it builds, loads, exports every function include/lmoe.h declares,
+and rejects bad arguments on the host before touching the GPU.  CPU only."""
+import ctypes
+import os
+
+import pytest
+
+from sparse_moe_layer_cutoff_b300 import lmoe as L
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        from sparse_moe_layer_cutoff_b300 import build
+        build.build()
+    return L.load_library()
+
+
+def test_exports_every_declared_symbol(lib):
+    syms = L.declared_symbols()
+    assert {"lmoe_create", "lmoe_route", "lmoe_forward", "lmoe_destroy"} <= set(syms)
+    for s in syms:
+        assert hasattr(lib, s), s
+
+
+def test_status_strings(lib):
+    for code, name in enumerate(["LMOE_OK", "LMOE_ERR_INVALID_ARG", "LMOE_ERR_UNSUPPORTED", "LMOE_ERR_OOM",
+                                 "LMOE_ERR_CUDA", "LMOE_ERR_TIMEOUT", "LMOE_ERR_DEVICE_ASSERT"]):
+        assert L.lmoe_status_string(code) == name
+    assert L.lmoe_status_string(99) == "LMOE_ERR_UNKNOWN"
+
+
+def test_struct_layout_matches_header(lib):
+    assert ctypes.sizeof(L.lmoe_config) == 11 * 4
+    assert ctypes.sizeof(L.lmoe_weights) == 11 * 8
+
+
+def _cfg(**kw):
+    base = dict(d=1024, latent=256, n_experts=64, top_k=8, expert_inter=512, n_shared=2, shared_inter=1024,
+                beta=4.0, beta_u=25.0, rms_eps=1e-6, dtype=L.LMOE_BF16)
+    base.update(kw)
+    return L.lmoe_config(*[base[f] for f, _ in L.lmoe_config._fields_])
+
+
+def _weights(ptr=0x10000, **kw):
+    w = L.lmoe_weights()
+    for n, _ in L.lmoe_weights._fields_:
+        setattr(w, n, None if n == "router_bias" else ptr)
+    for k, v in kw.items():
+        setattr(w, k, v)
+    return w
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(d=0), L.LMOE_ERR_INVALID_ARG),
+    (dict(top_k=65, n_experts=100), L.LMOE_ERR_UNSUPPORTED),
+    (dict(top_k=9, n_experts=8), L.LMOE_ERR_INVALID_ARG),
+    (dict(n_experts=5000), L.LMOE_ERR_UNSUPPORTED),
+    (dict(n_shared=4), L.LMOE_ERR_UNSUPPORTED),
+    (dict(d=1000), L.LMOE_ERR_UNSUPPORTED),          # bf16 tiles need multiples of 64
+    (dict(expert_inter=96), L.LMOE_ERR_UNSUPPORTED),
+    (dict(dtype=7), L.LMOE_ERR_INVALID_ARG),
+    (dict(beta=0.0), L.LMOE_ERR_INVALID_ARG),
+    (dict(beta_u=float("nan")), L.LMOE_ERR_INVALID_ARG),
+    (dict(rms_eps=-1.0), L.LMOE_ERR_INVALID_ARG),
+    (dict(dtype=L.LMOE_F32, latent=62), L.LMOE_ERR_UNSUPPORTED),
+])
+def test_create_rejects_bad_config(lib, kw, status):
+    st, ctx = L.lmoe_create(_cfg(**kw), _weights(), 16)
+    assert st == status and ctx is None
+
+
+def test_create_rejects_bad_weights_and_sizes(lib):
+    assert L.lmoe_create(_cfg(), _weights(w_down=None), 16)[0] == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_create(_cfg(), _weights(exp_up=0x10008), 16)[0] == L.LMOE_ERR_INVALID_ARG   # misaligned
+    assert L.lmoe_create(_cfg(), _weights(router_bias=0x10004), 16)[0] == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_create(_cfg(), _weights(), 0)[0] == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_create(_cfg(), _weights(), -3)[0] == L.LMOE_ERR_INVALID_ARG
+    out = ctypes.c_void_p()
+    assert lib.lmoe_create(None, ctypes.byref(_weights()), 16, None, ctypes.byref(out)) == L.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_create(ctypes.byref(_cfg()), None, 16, None, ctypes.byref(out)) == L.LMOE_ERR_INVALID_ARG
+    assert lib.lmoe_create(ctypes.byref(_cfg()), ctypes.byref(_weights()), 16, None, None) == L.LMOE_ERR_INVALID_ARG
+
+
+def test_calls_on_null_context(lib):
+    assert L.lmoe_route(None, 0x1000, 4) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_forward(None, 0x1000, 4, 0x2000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_sync_status(None) == L.LMOE_ERR_INVALID_ARG
+    with pytest.raises(L.LmoeError):
+        L.lmoe_workspace(None)
+    L.lmoe_destroy(None)   # no-op

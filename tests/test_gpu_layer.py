@@ -1,0 +1,197 @@
+"""Parity of the CUDA layer with the fp64 oracle (GPU).
+
+Routing (expert ids, per-expert counts, segments) is compared bit-exactly given the
+library's own fp32 logits; cutoffs to 1e-15 and combine weights to 1e-6 relative; the
+layer output within max-abs 2e-2 and relative L2 1e-2 (bf16) or relative L2 1e-5 (fp32)."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import lmoe_oracle as O
+from sparse_moe_layer_cutoff_b300 import LatentMoE, LmoeError
+from sparse_moe_layer_cutoff_b300 import lmoe as L
+from tests.lmoe_testing import Run, oracle_weights, rel_l2, to64
+from workloads import WORKLOADS, LayerShape, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SMALL = WORKLOADS["small_bf16"].shape
+
+
+@pytest.fixture(autouse=True)
+def _free():
+    yield
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def test_tiny_f32_layer_matches_oracle():
+    r = Run(WORKLOADS["tiny_f32"])
+    assert r.status == 0
+    r.check_logits(rtol=1e-6)
+    r.check_output()
+
+
+def test_small_bf16_layer_matches_oracle():
+    r = Run(WORKLOADS["small_bf16"])
+    assert r.status == 0
+    r.check_logits()
+    m, rl = r.check_output()
+    assert rl < BF16_TIGHT, rl
+
+
+BF16_TIGHT = 1e-2
+
+
+def test_small_bf16_stages_match_oracle():
+    """Each intermediate against the oracle's fp64 value of the same stage."""
+    r = Run(WORKLOADS["small_bf16"], bt=300)
+    s = r.shape
+    ref = r.check_routing()
+    W = oracle_weights(r.weights)
+    x64 = to64(r.x)
+    z_ref = x64 @ W["w_down"].T
+    assert rel_l2(to64(r.ws["z"]), z_ref) < 4e-3
+    # expert activations and outputs, slot by slot, for a sample of slots
+    rng = np.random.default_rng(0)
+    slots = rng.choice(r.bt * s.top_k, size=64, replace=False)
+    off = ref["offsets"]
+    h = to64(r.ws["h"][torch.as_tensor(slots, device="cuda")])
+    y = to64(r.ws["y"][torch.as_tensor(slots, device="cuda")])
+    for i, slot in enumerate(slots):
+        e = int(np.searchsorted(off, slot, side="right") - 1)
+        t = ref["perm"][slot]
+        a = O.situ_glu(W["exp_gate"][e] @ z_ref[t], W["exp_up"][e] @ z_ref[t], s.beta, s.beta_u)
+        assert rel_l2(h[i], a) < 2e-2
+        assert rel_l2(y[i], W["exp_down"][e] @ a) < 2e-2
+    # the combined latent and the shared activations
+    c_ref = O.routed_latent(z_ref, ref["idx"], ref["w"], W, s.beta, s.beta_u, s.rms_eps)
+    cat = to64(r.ws["cat"])
+    assert rel_l2(cat[:, : s.latent], c_ref) < 2e-2
+    for j in range(s.n_shared):
+        a = O.situ_glu(x64 @ W["sh_gate"][j].T, x64 @ W["sh_up"][j].T, s.beta, s.beta_u)
+        got = cat[:, s.latent + j * s.shared_inter: s.latent + (j + 1) * s.shared_inter]
+        assert rel_l2(got, a) < 1e-2
+
+
+@pytest.mark.parametrize("bt", [1, 3, 129, 200, 1000])
+def test_ragged_token_counts(bt):
+    r = Run(WORKLOADS["small_bf16"], bt=bt)
+    assert r.status == 0
+    r.check_output()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(n_experts=24, top_k=5),            # E not a multiple of 32
+    dict(n_experts=8, top_k=8),             # K = E: every expert takes every token
+    dict(n_experts=200, top_k=1),
+    dict(n_experts=64, top_k=33),           # K above one warp
+    dict(n_shared=1), dict(n_shared=3),
+    dict(latent=192, expert_inter=320, shared_inter=448),
+])
+def test_shape_variants(kw):
+    shape = LayerShape(**{**SMALL.__dict__, **kw})
+    w = Workload("variant", shape, 333, 11, gamma_noise=0.1)
+    r = Run(w)
+    assert r.status == 0
+    r.check_output()
+
+
+def test_tiny_f32_variants():
+    shape = LayerShape(d=96, latent=20, n_experts=7, top_k=3, expert_inter=36, n_shared=2, shared_inter=28,
+                       dtype="f32")
+    r = Run(Workload("f32v", shape, 77, 5, gamma_noise=0.2))
+    r.check_output()
+
+
+def test_zero_input_routes_to_first_experts_and_outputs_zero():
+    x, weights, _ = make_inputs(WORKLOADS["small_bf16"], "cuda", 130)
+    x.zero_()
+    r = Run(WORKLOADS["small_bf16"], x=x, weights=weights)
+    K = r.shape.top_k
+    assert torch.equal(r.route["idx"].cpu(), torch.arange(K, dtype=torch.int32).repeat(130, 1))
+    assert torch.all(r.route["w"] == 1.0 / K)
+    assert torch.count_nonzero(r.out).item() == 0
+
+
+def test_skewed_routing_small():
+    """Zipf logit bias and a block of identical tokens on the small shape."""
+    w = WORKLOADS["small_bf16"].with_(zipf_bias=True, repeat_frac=0.25, seed=4)
+    r = Run(w)
+    r.check_output()
+    nrep = int(round(r.bt * 0.25))
+    assert torch.equal(r.out[:nrep], r.out[:1].expand(nrep, -1))
+
+
+def test_repeat_calls_are_bit_identical():
+    r = Run(WORKLOADS["small_bf16"], bt=500)
+    again = r.layer.forward(r.x)
+    torch.cuda.synchronize()
+    assert torch.equal(again, r.out)
+
+
+def test_max_bt_larger_than_bt_and_reuse():
+    """One context serves batches of several sizes."""
+    x, weights, _ = make_inputs(WORKLOADS["small_bf16"], "cuda", 700)
+    layer = LatentMoE(SMALL, weights, max_bt=1024)
+    for bt in (700, 64, 1, 513):
+        out = layer.forward(x[:bt].contiguous())
+        torch.cuda.synchronize()
+        ref_r = Run(WORKLOADS["small_bf16"], x=x[:bt].contiguous(), weights=weights)
+        assert torch.equal(out, ref_r.out)
+    assert layer.sync_status() == 0
+
+
+def test_argument_errors_on_device():
+    x, weights, _ = make_inputs(WORKLOADS["small_bf16"], "cuda", 16)
+    layer = LatentMoE(SMALL, weights, max_bt=16)
+    assert L.lmoe_forward(layer.ctx, x.data_ptr(), 17, x.data_ptr() + 4096) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_forward(layer.ctx, x.data_ptr(), 8, x.data_ptr()) == L.LMOE_ERR_INVALID_ARG  # out overlaps x
+    assert L.lmoe_forward(layer.ctx, x.data_ptr(), 0, 0) == L.LMOE_OK                          # bt = 0
+    assert L.lmoe_route(layer.ctx, x.data_ptr(), -1) == L.LMOE_ERR_INVALID_ARG
+    # host memory is not accepted as a weight
+    cpu_w = dict(weights)
+    cpu_w["w_up"] = weights["w_up"].cpu()
+    with pytest.raises(LmoeError) as ei:
+        LatentMoE(SMALL, cpu_w, max_bt=16)
+    assert ei.value.status == L.LMOE_ERR_INVALID_ARG
+
+
+# --------------------------------------------------------------------------- full shape
+
+def _sample_rows(bt, extra=()):
+    rng = np.random.default_rng(bt)
+    rows = {0, 1, bt // 2, bt - 1, *extra}
+    rows |= set(rng.choice(bt, size=min(bt, 4), replace=False).tolist())
+    return sorted(rows)
+
+
+def test_full_decode_bt64():
+    r = Run(WORKLOADS["full_decode_bt64"])
+    assert r.status == 0
+    ref = r.check_routing()
+    r.check_logits(rows=[0, 17, 63])
+    r.check_output(rows=_sample_rows(r.bt), ref_route=ref)
+
+
+@pytest.mark.slow
+def test_full_prefill_bt8192():
+    r = Run(WORKLOADS["full_prefill_bt8192"])
+    assert r.status == 0
+    ref = r.check_routing()
+    r.check_logits(rows=[0, 4097, 8191])
+    r.check_output(rows=_sample_rows(r.bt), ref_route=ref)
+    r.close()
+
+
+@pytest.mark.slow
+def test_full_skewed_bt16384():
+    r = Run(WORKLOADS["full_skewed_bt16384"])
+    assert r.status == 0
+    ref = r.check_routing()
+    counts = ref["counts"]
+    assert counts.max() >= 4096      # the repeated block lands on K experts together
+    r.check_output(rows=_sample_rows(r.bt, extra=(100, 5000)), ref_route=ref)
+    nrep = r.bt // 4
+    assert torch.equal(r.out[:nrep], r.out[:1].expand(nrep, -1))
+    r.close()
