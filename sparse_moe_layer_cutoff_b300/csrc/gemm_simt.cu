@@ -38,7 +38,7 @@ gemm_simt_kernel(const GemmArgs a) {
     int lo = 0, hi = a.G;                       // largest g with mtile_off[g] <= mt
     while (hi - lo > 1) { int mid = (lo + hi) >> 1; if (a.mtile_off[mid] <= mt) lo = mid; else hi = mid; }
     g = lo;
-    row0 = a.seg_off[g] + (mt - a.mtile_off[g]) * kSBM;
+    row0 = a.seg_off[g] + (mt - a.mtile_off[g]) * kTileM + blockIdx.z * kSBM;  // kTileM = 2 * kSBM
     row_end = a.seg_off[g + 1];
   } else {
     row0 = blockIdx.y * kSBM;
@@ -121,7 +121,8 @@ gemm_simt_kernel(const GemmArgs a) {
 
 template <typename T>
 static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
-  dim3 grid((a.N + kSBN - 1) / kSBN, a.seg_off ? a.max_mtiles : (a.M + kSBM - 1) / kSBM);
+  static_assert(kTileM == 2 * kSBM, "grouped tiles are two CUDA-core row blocks");
+  dim3 grid((a.N + kSBN - 1) / kSBN, a.seg_off ? a.max_mtiles : (a.M + kSBM - 1) / kSBM, a.seg_off ? 2 : 1);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   switch (a.epi) {
     case kEpiStore: gemm_simt_kernel<T, kEpiStore><<<grid, kSThreads, 0, st>>>(a); break;

@@ -1,11 +1,620 @@
+// Tensor-core engine of the bf16 layer: one persistent, warp-specialised tcgen05 GEMM
+// kernel serves every contraction ("Stable LatentMoE": router, down_proj, GroupedExperts
+// gate/up + SiTU-GLU, expert down, shared experts, up_proj + shared down).
+//
+// Weight-stationary tiles: the MMA's M = 128 side is 128 weight rows (output features),
+// its N side is up to 256 tokens, K steps of 64 (one 128-byte swizzle row of bf16).
+//   * tokens of one expert segment are covered by token tiles of 256 and one last tile
+//     rounded up to a multiple of 16, so an expert with 146 tokens wastes 14 MMA columns
+//     instead of the 110 rows a 128-row token tile would;
+//   * each weight tile is streamed from HBM once per token tile (one tile per expert at
+//     prefill sizes), which is what bounds the layer;
+//   * the GLU tiles hold 64 gate rows and the matching 64 up rows, so one accumulator
+//     has both branches and the epilogue pairs them through shared memory.
+// Roles (192 threads): warp 0 issues TMA loads into a 4-stage ring, warp 1 owns TMEM and
+// issues tcgen05.mma (one thread), warps 2-5 drain the double-buffered accumulators
+// (2 x 256 TMEM columns) with tcgen05.ld and write the outputs.  Every mbarrier wait is
+// bounded: on expiry the kernel records LMOE timeout status, drains what it issued and
+// returns.
+#include <cuda.h>
+
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
 #include "gemm_tc.h"
 
 namespace lmoe {
-struct TcPlan { int unused; };
-lmoe_status tc_plan_create(const lmoe_config*, const lmoe_weights*, int, int, const TcBuffers&, TcPlan** plan) {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBK = 64;
+constexpr int kFeat = 128;
+constexpr int kTokMax = 256;
+constexpr int kTokBox = 16;
+constexpr int kAccCols = 256;
+constexpr int kStageW = kFeat * kBK * 2;     // 16 KB of weights per stage
+constexpr int kStageT = kTokMax * kBK * 2;   // 32 KB of tokens per stage
+constexpr int kThreads = 192;
+constexpr int kXStride = 17;                 // floats per exchange row (bank padding)
+constexpr int kXBuf = 2 * 64 * kXStride;     // floats per exchange buffer (gate + up halves)
+constexpr int kXchgBytes = 2 * kXBuf * 4;
+constexpr int kDenseGroup = 8;               // token tiles per raster group (dense GEMMs)
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr int kSmemBytes = 1024 + kStages * (kStageW + kStageT) + kXchgBytes + kNumBars * 8 + 16;
+constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
+
+struct TcMaps {
+  CUtensorMap w[kMaxKSeg];  // weight (MMA A) maps, one per K segment; GLU: w[0] = gate
+  CUtensorMap wup;          // GLU up-branch weights
+  CUtensorMap tok;          // token (MMA B) rows, 16-row boxes
+};
+
+struct TcParams {
+  int nseg;
+  int seg_k0[kMaxKSeg + 1];
+  int seg_row0[kMaxKSeg];
+  int w_group_rows;         // weight rows per group (routed experts), 0 for dense
+  int n_feat;               // output features
+  int n_fb;                 // feature blocks (128 rows, or 64 outputs for GLU)
+  int kblocks;              // K / 64
+  int bt;                   // dense: tokens
+  const int32_t* seg_off;   // grouped: [G + 1] token segments
+  const int32_t* mtile_off; // grouped: [G + 1] prefix of 256-token tiles
+  int G;
+  void* out;
+  long long ldo;
+  float* out_t;
+  long long ldt;
+  const float* bias;
+  float beta, beta_u;
+  uint32_t* status;
+};
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait.  Gives up when the deadline passes (setting abort + timeout status) or,
+// if honour_abort, as soon as another role has aborted.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                       uint32_t* status, bool honour_abort = true) {
+  if (mbar_test(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_test(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (honour_abort && *abort_flag) return false;
+      if (global_ns() - t0 > kTimeoutNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns of TMEM (this warp's lane quadrant).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes
+// in 8-row (1024-byte) groups; start address advanced by 32 bytes per K step of 16.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 accumulator.
+__device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Barrier over the epilogue warps that also ORs a flag across them.
+__device__ __forceinline__ bool named_sync_or(int id, int n, bool flag) {
+  uint32_t res;
+  asm volatile(
+      "{\n\t.reg .pred q, r;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred r, %2, %3, q;\n\tselp.u32 %0, 1, 0, r;\n}"
+      : "=r"(res)
+      : "r"((uint32_t)flag), "r"(id), "r"(n)
+      : "memory");
+  return res != 0;
+}
+
+// ------------------------------------------------------------------ tile schedule
+struct Tile {
+  int g, fb, tok0, ntok;
+};
+
+__device__ __forceinline__ int num_tiles(const TcParams& p) {
+  if (p.seg_off) return p.mtile_off[p.G] * p.n_fb;
+  return ((p.bt + kTokMax - 1) / kTokMax) * p.n_fb;
+}
+
+// Grouped: tiles ordered (expert, feature block, token tile) so the CTAs working at the
+// same time share weight tiles and token rows in L2.  Dense: token tiles in groups of
+// kDenseGroup, feature blocks inside a group.
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
+  Tile r;
+  if (p.seg_off) {
+    const int q = t / p.n_fb;
+    int lo = 0, hi = p.G;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.mtile_off[mid] <= q) lo = mid; else hi = mid;
+    }
+    const int m0 = p.mtile_off[lo];
+    const int nt = p.mtile_off[lo + 1] - m0;
+    const int local = t - m0 * p.n_fb;
+    r.g = lo;
+    r.fb = local / nt;
+    const int tb = local - r.fb * nt;
+    r.tok0 = p.seg_off[lo] + tb * kTokMax;
+    r.ntok = min(kTokMax, p.seg_off[lo + 1] - r.tok0);
+  } else {
+    const int nt = (p.bt + kTokMax - 1) / kTokMax;
+    const int grp = t / (kDenseGroup * p.n_fb);
+    const int in = t - grp * kDenseGroup * p.n_fb;
+    const int gcnt = min(kDenseGroup, nt - grp * kDenseGroup);
+    r.g = 0;
+    r.fb = in / gcnt;
+    const int tb = grp * kDenseGroup + (in - r.fb * gcnt);
+    r.tok0 = tb * kTokMax;
+    r.ntok = min(kTokMax, p.bt - r.tok0);
+  }
+  return r;
+}
+
+// ------------------------------------------------------------------ the kernel
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw);
+  const uint32_t wbase = base;
+  const uint32_t tbase = base + kStages * kStageW;
+  float* xchg = reinterpret_cast<float*>(sbase + kStages * (kStageW + kStageT));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + kStages * (kStageW + kStageT) + kXchgBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 128); }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(2 * kAccCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = num_tiles(p);
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t pending = 0;                       // stages with loads not yet re-acquired
+    uint32_t pend_parity = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+      const Tile tl = decode_tile(p, t);
+      const int ntr = (tl.ntok + 15) & ~15;
+      const uint32_t bytes = kStageW + (uint32_t)ntr * (kBK * 2);
+      const int nbox = ntr / kTokBox;
+      for (int kb = 0; kb < p.kblocks; ++kb) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { stop = true; break; }
+        pending &= ~(1u << stage);
+        if (lane == 0) mbar_expect_tx(full_bar(stage), bytes);
+        __syncwarp();
+        const uint32_t wdst = wbase + stage * kStageW, tdst = tbase + stage * kStageT;
+        const int k = kb * kBK;
+        if (lane == 0) {
+          if (EPI == kEpiGlu) {
+            const int row = tl.g * p.w_group_rows + tl.fb * 64;
+            tma_load_2d(wdst, &maps.w[0], k, row, full_bar(stage));
+            tma_load_2d(wdst + 64 * kBK * 2, &maps.wup, k, row, full_bar(stage));
+          } else {
+            int s = 0;
+#pragma unroll
+            for (int i = 1; i < kMaxKSeg; ++i)
+              if (i < p.nseg && k >= p.seg_k0[i]) s = i;
+            const int row = p.seg_row0[s] + tl.g * p.w_group_rows + tl.fb * kFeat;
+            tma_load_2d(wdst, &maps.w[s], k - p.seg_k0[s], row, full_bar(stage));
+          }
+        }
+        if (lane < nbox) tma_load_2d(tdst + lane * (kTokBox * kBK * 2), &maps.tok, k, tl.tok0 + lane * kTokBox,
+                                     full_bar(stage));
+        pending |= 1u << stage;
+        pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (stop && lane == 0) {
+      // no copy may still be landing in shared memory when the block exits
+      for (int s = 0; s < kStages; ++s)
+        if (pending & (1u << s)) mbar_wait(full_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, false);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool stop = false, issued = false;
+      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+        const Tile tl = decode_tile(p, t);
+        const int ntr = (tl.ntok + 15) & ~15;
+        const uint32_t idesc = idesc_bf16(kFeat, ntr);
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { stop = true; break; }
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { stop = true; break; }
+          tc_fence_after();
+          const uint64_t ad = smem_desc(wbase + stage * kStageW);
+          const uint64_t bd = smem_desc(tbase + stage * kStageT);
+#pragma unroll
+          for (int j = 0; j < kBK / 16; ++j)
+            tc_mma(d, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+          issued = true;
+          tc_commit(empty_bar(stage));
+          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        }
+        if (stop) break;
+        tc_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      }
+      if (stop && issued) {
+        tc_commit(drain_bar);
+        mbar_wait(drain_bar, 0, abort_flag, p.status, false);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------------- epilogue
+    const int q = warp & 3;                 // TMEM lane quadrant of this warp
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int chunk_ctr = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Tile tl = decode_tile(p, t);
+      const bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status);
+      if (named_sync_or(2, 128, !ok || *abort_flag)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
+      const int nchunks = (tl.ntok + 31) / 32;
+      if (EPI == kEpiGlu) {
+        const int r64 = (q & 1) * 32 + lane;       // row inside the gate (q 0,1) or up (q 2,3) half
+        const int fout = tl.fb * 64 + r64;
+        bf16* out = static_cast<bf16*>(p.out);
+        for (int c = 0; c < nchunks; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          float* xg = xchg + (chunk_ctr & 1) * kXBuf;
+          float* xu = xg + 64 * kXStride;
+          if (q < 2) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xg[r64 * kXStride + j] = v[16 + j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) xu[r64 * kXStride + j] = v[j];
+          }
+          named_sync(1, 128);
+          const int jb = c * 32 + (q < 2 ? 0 : 16);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float gv = q < 2 ? v[j] : xg[r64 * kXStride + j];
+            const float uv = q < 2 ? xu[r64 * kXStride + j] : v[16 + j];
+            const int tok = jb + j;
+            if (tok < tl.ntok && fout < p.n_feat)
+              out[(long long)(tl.tok0 + tok) * p.ldo + fout] = __float2bfloat16_rn(situ_glu(gv, uv, p.beta, p.beta_u));
+          }
+          ++chunk_ctr;
+        }
+      } else {
+        const int fout = tl.fb * kFeat + q * 32 + lane;
+        const bool fok = fout < p.n_feat;
+        const float bias = (EPI == kEpiRouter && fok && p.bias) ? p.bias[fout] : 0.f;
+        for (int c = 0; c < nchunks; ++c) {
+          float v[32];
+          tmem_ld32(taddr + c * 32, v);
+          if (!fok) continue;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int tok = c * 32 + j;
+            if (tok < tl.ntok) {
+              const long long row = tl.tok0 + tok;
+              if (EPI == kEpiStore) {
+                static_cast<bf16*>(p.out)[row * p.ldo + fout] = __float2bfloat16_rn(v[j]);
+              } else {
+                const float val = v[j] + bias;
+                static_cast<float*>(p.out)[row * p.ldo + fout] = val;
+                p.out_t[(long long)fout * p.ldt + row] = val;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols));
+}
+
+// Routed-expert token rows in slot order: zp[slot] = z[perm[slot]] (16-byte vectors).
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ z, const int32_t* __restrict__ perm,
+                                                          const int32_t* __restrict__ offsets, int n_experts,
+                                                          int vec_per_row, uint4* __restrict__ zp) {
+  const long long nslots = offsets[n_experts];
+  const long long total = nslots * vec_per_row;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const long long slot = i / vec_per_row;
+    const int v = (int)(i - slot * vec_per_row);
+    zp[i] = z[(long long)perm[slot] * vec_per_row + v];
+  }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    cudaGetLastError();
+  }
+  return fn;
+}
+
+// 2-D bf16 map over rows x cols (row stride ld elements), box 64 columns x box_rows rows,
+// 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_rows) {
+  EncodeTiledFn enc = encoder();
+  if (!enc || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+struct TcPlan {
+  lmoe_config cfg;
+  int max_bt;
+  int sm_count;
+  TcBuffers buf;
+  CUtensorMap m_router, m_down, m_gate, m_up, m_edown, m_shg, m_shu, m_wup, m_shd;  // weights
+  CUtensorMap m_zp, m_h, m_cat;                                                       // workspace
+};
+
+lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int max_bt, int sm_count,
+                           const TcBuffers& buf, TcPlan** plan) {
   *plan = nullptr;
+  TcPlan* pl = new (std::nothrow) TcPlan();
+  if (!pl) return LMOE_ERR_OOM;
+  pl->cfg = *cfg;
+  pl->max_bt = max_bt;
+  pl->sm_count = sm_count;
+  pl->buf = buf;
+  const lmoe_config& c = *cfg;
+  const long long E = c.n_experts, d = c.d, L = c.latent, I = c.expert_inter, S = c.n_shared, Is = c.shared_inter;
+  const long long ldc = L + S * Is;
+  const long long slots = (long long)max_bt * c.top_k;
+  bool ok = make_map(&pl->m_router, w->w_router, E, d, d, kFeat) && make_map(&pl->m_down, w->w_down, L, d, d, kFeat) &&
+            make_map(&pl->m_gate, w->exp_gate, E * I, L, L, 64) && make_map(&pl->m_up, w->exp_up, E * I, L, L, 64) &&
+            make_map(&pl->m_edown, w->exp_down, E * L, I, I, kFeat) &&
+            make_map(&pl->m_shg, w->sh_gate, S * Is, d, d, 64) && make_map(&pl->m_shu, w->sh_up, S * Is, d, d, 64) &&
+            make_map(&pl->m_wup, w->w_up, d, L, L, kFeat) && make_map(&pl->m_shd, w->sh_down, S * d, Is, Is, kFeat) &&
+            make_map(&pl->m_zp, buf.zp, slots, L, L, kTokBox) && make_map(&pl->m_h, buf.h, slots, I, I, kTokBox) &&
+            make_map(&pl->m_cat, buf.cat, max_bt, ldc, ldc, kTokBox);
+  if (!ok) {
+    delete pl;
+    return LMOE_ERR_CUDA;
+  }
+  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiStore>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiRouter>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete pl;
+    return LMOE_ERR_CUDA;
+  }
+  *plan = pl;
   return LMOE_OK;
 }
-void tc_plan_destroy(TcPlan*) {}
-cudaError_t launch_gemm_tc(TcPlan*, const GemmArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+
+void tc_plan_destroy(TcPlan* plan) { delete plan; }
+
+int tc_launches(int op) { return op == kOpExpertGateUp ? 2 : 1; }
+
+cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
+  const lmoe_config& c = pl->cfg;
+  TcMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  p.nseg = 1;
+  p.seg_k0[0] = 0;
+  p.seg_k0[1] = a.K;
+  p.n_feat = a.N;
+  p.kblocks = a.K / kBK;
+  p.out = a.out;
+  p.ldo = a.ldo;
+  p.beta = a.beta;
+  p.beta_u = a.beta_u;
+  p.status = pl->buf.status;
+  int epi = a.epi;
+  bool ok = true;
+  switch (a.op) {
+    case kOpRouter:
+      maps.w[0] = pl->m_router;
+      ok = make_map(&maps.tok, a.A, a.M, a.K, a.lda, kTokBox);
+      p.bt = a.M;
+      p.out_t = a.out_t;
+      p.ldt = a.ldt;
+      p.bias = a.bias;
+      break;
+    case kOpDown:
+      maps.w[0] = pl->m_down;
+      ok = make_map(&maps.tok, a.A, a.M, a.K, a.lda, kTokBox);
+      p.bt = a.M;
+      break;
+    case kOpSharedGateUp:
+      maps.w[0] = pl->m_shg;
+      maps.wup = pl->m_shu;
+      ok = make_map(&maps.tok, a.A, a.M, a.K, a.lda, kTokBox);
+      p.bt = a.M;
+      break;
+    case kOpFinal:
+      maps.w[0] = pl->m_wup;
+      maps.tok = pl->m_cat;
+      p.bt = a.M;
+      p.nseg = a.nseg;
+      for (int s = 0; s < a.nseg; ++s) {
+        if (s > 0) maps.w[s] = pl->m_shd;
+        p.seg_k0[s] = a.seg_k0[s];
+        p.seg_row0[s] = (int)a.seg_row0[s];
+      }
+      p.seg_k0[a.nseg] = a.K;
+      break;
+    case kOpExpertGateUp: {
+      // token rows of each expert segment, gathered once into slot order
+      const int vec = c.latent / 8;
+      gather_rows_kernel<<<pl->sm_count * 8, 256, 0, st>>>(static_cast<const uint4*>(pl->buf.z), a.a_rows, a.seg_off,
+                                                           a.G, vec, static_cast<uint4*>(pl->buf.zp));
+      maps.w[0] = pl->m_gate;
+      maps.wup = pl->m_up;
+      maps.tok = pl->m_zp;
+      p.w_group_rows = c.expert_inter;
+      p.seg_off = a.seg_off;
+      p.mtile_off = a.mtile_off;
+      p.G = a.G;
+      break;
+    }
+    case kOpExpertDown:
+      maps.w[0] = pl->m_edown;
+      maps.tok = pl->m_h;
+      p.w_group_rows = c.latent;
+      p.seg_off = a.seg_off;
+      p.mtile_off = a.mtile_off;
+      p.G = a.G;
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  p.n_fb = epi == kEpiGlu ? (a.N + 63) / 64 : (a.N + kFeat - 1) / kFeat;
+  int grid = pl->sm_count;
+  if (!p.seg_off) {
+    const long long tiles = (long long)((p.bt + kTokMax - 1) / kTokMax) * p.n_fb;
+    if (tiles < grid) grid = (int)tiles;
+  }
+  if (grid <= 0) return cudaSuccess;
+  switch (epi) {
+    case kEpiStore: tc_gemm_kernel<kEpiStore><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+    case kEpiGlu: tc_gemm_kernel<kEpiGlu><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+    default: tc_gemm_kernel<kEpiRouter><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace lmoe

@@ -10,6 +10,7 @@ struct TcPlan;  // tensor maps of the borrowed weights and of the workspace, lau
 
 struct TcBuffers {
   void* z;
+  void* zp;          // [max_bt * K, latent] routed token rows in slot order
   void* h;
   void* y;
   void* cat;
@@ -22,5 +23,6 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int ma
                            const TcBuffers& buf, TcPlan** plan);
 void tc_plan_destroy(TcPlan* plan);
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
+int tc_launches(int op);   // kernels launch_gemm_tc starts for one GemmOp
 
 }  // namespace lmoe

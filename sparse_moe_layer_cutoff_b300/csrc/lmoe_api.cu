@@ -42,6 +42,7 @@ struct lmoe_ctx {
   int32_t* perm;
   int32_t* inv;
   void* z;
+  void* zp;
   void* h;
   void* y;
   void* cat;
@@ -122,7 +123,7 @@ lmoe_status finish(lmoe_ctx* ctx, cudaStream_t st, cudaError_t e) {
 }
 
 cudaError_t run_gemm(lmoe_ctx* ctx, const GemmArgs& g, cudaStream_t st) {
-  ctx->launches += 1;
+  ctx->launches += ctx->use_tc ? tc_launches(g.op) : 1;
   if (ctx->use_tc) return launch_gemm_tc(ctx->tc, g, st);
   return launch_gemm_simt(g, ctx->bf16, st);
 }
@@ -238,6 +239,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   size_t o_inv = cv.take<int32_t>(bt * K);
   size_t o_status = cv.take<uint32_t>(4);
   size_t o_z = cv.take<char>(bt * L * ctx->esz);
+  size_t o_zp = ctx->bf16 ? cv.take<char>(bt * K * L * ctx->esz) : 0;
   size_t o_h = cv.take<char>(bt * K * c.expert_inter * ctx->esz);
   size_t o_y = cv.take<char>(bt * K * L * ctx->esz);
   size_t o_cat = cv.take<char>(bt * ldc * ctx->esz);
@@ -261,6 +263,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   ctx->inv = (int32_t*)(b + o_inv);
   ctx->status = (uint32_t*)(b + o_status);
   ctx->z = b + o_z;
+  ctx->zp = ctx->bf16 ? b + o_zp : nullptr;
   ctx->h = b + o_h;
   ctx->y = b + o_y;
   ctx->cat = b + o_cat;
@@ -276,7 +279,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
     const char* force = getenv("LMOE_FORCE_SIMT");
     if (!(force && force[0] == '1')) {
       TcBuffers tb;
-      tb.z = ctx->z; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
+      tb.z = ctx->z; tb.zp = ctx->zp; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
       tb.status = ctx->status;
       lmoe_status ts = tc_plan_create(&c, w, max_bt, ctx->sm_count, tb, &ctx->tc);
       if (ts != LMOE_OK) {
@@ -328,7 +331,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
   cudaError_t e = route_impl(ctx, x, bt, st, nullptr);
   prof_mark(ctx, 2, st);
   const long long ldc = (long long)c.latent + (long long)c.n_shared * c.shared_inter;
-  const int max_mtiles = (int)(((long long)bt * c.top_k) / kTileM + c.n_experts + 1);
+  const int max_mtiles = (int)(((long long)bt * c.top_k) / kTileM + c.n_experts + 1);  // >= sum of ceil(cnt/kTileM)
 
   if (e == cudaSuccess) {  // z = x W_down^T
     GemmArgs g = base_args(ctx);

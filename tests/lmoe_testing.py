@@ -103,7 +103,11 @@ class Run:
         return O.layer_forward(to64(self.x[rows]), ref_route["idx"][rows], ref_route["w"][rows],
                                oracle_weights(self.weights), s.beta, s.beta_u, s.rms_eps)
 
-    def check_output(self, rows=None, ref_route=None):
+    def check_output(self, rows=None, ref_route=None, scaled=False):
+        """Layer output against the oracle.  The bf16 bound is max-abs 2e-2 and rel-L2 1e-2;
+        with scaled=True (shapes other than the specified workloads, whose outputs can be
+        larger) the max-abs bound grows by the bf16 rounding of the output itself,
+        2^-8 * max|out| (one ulp)."""
         rows = np.arange(self.bt) if rows is None else np.asarray(rows)
         ref_route = ref_route or self.check_routing()
         ref = self.oracle_out(rows, ref_route)
@@ -113,5 +117,6 @@ class Run:
         if self.shape.dtype == "f32":
             assert r <= F32_REL_L2, (r, m)
         else:
-            assert m <= BF16_MAX_ABS and r <= BF16_REL_L2, (m, r)
+            bound = BF16_MAX_ABS + (2.0 ** -8 * float(np.abs(ref).max()) if scaled else 0.0)
+            assert m <= bound and r <= BF16_REL_L2, (m, r, bound)
         return m, r
