@@ -70,6 +70,9 @@ WORKLOADS = {
     "full_decode_bt64": Workload("full_decode_bt64", FULL, 64, 3),
     "full_skewed_bt16384": Workload("full_skewed_bt16384", FULL, 16384, 4, zipf_bias=True,
                                     repeat_frac=0.25),
+    # profiling case for counter captures: the full-width kernels with 32 experts (2.5 GB of
+    # weights, still far above L2) and ~148 tokens per expert, as at bt = 8192 with 896
+    "profile_e32_bt296": Workload("profile_e32_bt296", dataclasses.replace(FULL, n_experts=32), 296, 5),
 }
 
 
