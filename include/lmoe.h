@@ -178,6 +178,28 @@ LMOE_API lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* ou
 LMOE_API lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable);
 LMOE_API lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t* launches);
 
+/* Expert segments from given top-K ids, with no allocation by the library.
+ * The paper has no counterpart: this is a service to callers that cannot let a library
+ * call cudaMalloc, because their device memory belongs to another allocator (such as a
+ * framework's caching pool that has reserved the free HBM) or because cudaMalloc's
+ * implicit device synchronisation is not acceptable on their path.
+ * Computes exactly what lmoe_route leaves in its workspace: a stable counting sort of the
+ * bt*top_k (token, k) pairs of topk_idx [bt, top_k] (device, int32, ids in [0, n_experts))
+ * by expert, writing expert_counts [n_experts], offsets [n_experts + 1], perm [bt*top_k]
+ * (slot -> token) and inv [bt*top_k] ((t, k) -> slot), all caller-owned device buffers.
+ * Working memory is one fixed 4 MiB device array inside the library (held on every GPU
+ * that loads it until exit), so calls need
+ *   (ceil(bt / 128) * n_experts + 2 * n_experts + 1) * 4 bytes <= 4 MiB
+ * (e.g. bt <= 149,000 at n_experts = 896); larger calls return LMOE_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (once per device, with
+ * that device current); make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents: calls that overlap on
+ * the GPU (different streams, or different host threads, without ordering) race on it.
+ * bt == 0 returns LMOE_OK without launching. */
+LMOE_API lmoe_status lmoe_segments_noalloc(const int32_t* topk_idx, int32_t bt, int32_t top_k,
+                                           int32_t n_experts, int32_t* expert_counts, int32_t* offsets,
+                                           int32_t* perm, int32_t* inv, lmoe_stream stream);
+
 /* Library build identifier (static string): engine names per dtype. */
 LMOE_API const char* lmoe_build_info(void);
 

@@ -31,6 +31,10 @@ struct RouteArgs {
 constexpr int kRouteTailLaunches = 5;   // cutoff, top-K, count, scan, scatter
 cudaError_t route_tail_prepare();
 cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st);
+// Only the segmentation chain (count, scan, scatter) on caller-supplied buffers.
+cudaError_t launch_segments(const int32_t* idx, int bt, int top_k, int n_experts, int32_t* block_cnt,
+                            int32_t* counts, int32_t* offsets, int32_t* mtile_off, int32_t* perm, int32_t* inv,
+                            int32_t* user_counts, cudaStream_t st);
 
 // ---------------------------------------------------------------------------- GEMMs
 // C[r, n] = sum_k A[arow(r), k] * B(g, n, k), with

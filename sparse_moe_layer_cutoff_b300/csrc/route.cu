@@ -356,6 +356,19 @@ cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_segments(const int32_t* idx, int bt, int top_k, int n_experts, int32_t* block_cnt,
+                            int32_t* counts, int32_t* offsets, int32_t* mtile_off, int32_t* perm, int32_t* inv,
+                            int32_t* user_counts, cudaStream_t st) {
+  if (bt <= 0) return cudaSuccess;
+  const int nblk = (bt + kSegTokens - 1) / kSegTokens;
+  const size_t seg_smem = (size_t)kSegWarps * n_experts * sizeof(uint32_t);
+  seg_count_kernel<<<nblk, kSegThreads, seg_smem, st>>>(idx, bt, top_k, n_experts, block_cnt);
+  seg_scan_kernel<<<1, 1024, 2 * n_experts * sizeof(int32_t), st>>>(block_cnt, nblk, n_experts, kTileM, counts,
+                                                                    offsets, mtile_off, user_counts);
+  seg_scatter_kernel<<<nblk, kSegThreads, seg_smem, st>>>(idx, bt, top_k, n_experts, block_cnt, perm, inv);
+  return cudaGetLastError();
+}
+
 cudaError_t route_tail_prepare() {
   // dynamic shared memory above 48 KB for the largest supported expert count
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_profile_read.argtypes = [c_vp, ctypes.POINTER(c_f32), ctypes.POINTER(c_i32),
                                       ctypes.POINTER(ctypes.c_int64)]
     lib.lmoe_profile_read.restype = c_i32
+    lib.lmoe_segments_noalloc.argtypes = [c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp]
+    lib.lmoe_segments_noalloc.restype = c_i32
     lib.lmoe_build_info.argtypes = []
     lib.lmoe_build_info.restype = ctypes.c_char_p
     _lib = lib
@@ -145,6 +147,14 @@ def lmoe_profile_read(ctx):
     calls, launches = c_i32(), ctypes.c_int64()
     st = load_library().lmoe_profile_read(c_vp(ctx), ms, ctypes.byref(calls), ctypes.byref(launches))
     return st, dict(zip(STAGE_NAMES, list(ms))), calls.value, launches.value
+
+
+def lmoe_segments_noalloc(topk_idx: int, bt: int, top_k: int, n_experts: int, expert_counts: int, offsets: int,
+                          perm: int, inv: int, stream: int = 0) -> int:
+    """Expert segments from top-K ids using only the library's fixed scratch array (no
+    allocation); for callers whose device memory is managed by someone else."""
+    return load_library().lmoe_segments_noalloc(c_vp(topk_idx), bt, top_k, n_experts, c_vp(expert_counts),
+                                                c_vp(offsets), c_vp(perm), c_vp(inv), c_vp(stream))
 
 
 def lmoe_build_info() -> str:
