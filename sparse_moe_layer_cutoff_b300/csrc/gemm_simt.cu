@@ -38,8 +38,9 @@ gemm_simt_kernel(const GemmArgs a) {
     int lo = 0, hi = a.G;                       // largest g with mtile_off[g] <= mt
     while (hi - lo > 1) { int mid = (lo + hi) >> 1; if (a.mtile_off[mid] <= mt) lo = mid; else hi = mid; }
     g = lo;
-    row0 = a.seg_off[g] + (mt - a.mtile_off[g]) * kTileM + blockIdx.z * kSBM;  // kTileM = 2 * kSBM
-    row_end = a.seg_off[g + 1];
+    const int tile0 = a.seg_off[g] + (mt - a.mtile_off[g]) * kTileM;   // this m-tile: kTileM rows
+    row0 = tile0 + blockIdx.z * kSBM;                                    // at most 2 * kSBM
+    row_end = min(a.seg_off[g + 1], tile0 + kTileM);
   } else {
     row0 = blockIdx.y * kSBM;
     row_end = a.M;
@@ -121,7 +122,7 @@ gemm_simt_kernel(const GemmArgs a) {
 
 template <typename T>
 static cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
-  static_assert(kTileM == 2 * kSBM, "grouped tiles are two CUDA-core row blocks");
+  static_assert(kTileM <= 2 * kSBM, "a grouped m-tile spans at most two CUDA-core row blocks");
   dim3 grid((a.N + kSBN - 1) / kSBN, a.seg_off ? a.max_mtiles : (a.M + kSBM - 1) / kSBM, a.seg_off ? 2 : 1);
   if (grid.x == 0 || grid.y == 0) return cudaSuccess;
   switch (a.epi) {

@@ -2,19 +2,27 @@
 // kernel serves every contraction ("Stable LatentMoE": router, down_proj, GroupedExperts
 // gate/up + SiTU-GLU, expert down, shared experts, up_proj + shared down).
 //
-// Weight-stationary tiles: the MMA's M = 128 side is 128 weight rows (output features),
-// its N side is up to 256 tokens, K steps of 64 (one 128-byte swizzle row of bf16).
-//   * tokens of one expert segment are covered by token tiles of 256 and one last tile
-//     rounded up to a multiple of 16, so an expert with 146 tokens wastes 14 MMA columns
-//     instead of the 110 rows a 128-row token tile would;
-//   * each weight tile is streamed from HBM once per token tile (one tile per expert at
-//     prefill sizes), which is what bounds the layer;
-//   * the GLU tiles hold 64 gate rows and the matching 64 up rows, so one accumulator
-//     has both branches and the epilogue pairs them through shared memory.
-// Roles (192 threads): warp 0 issues TMA loads into a 4-stage ring, warp 1 owns TMEM and
-// issues tcgen05.mma (one thread), warps 2-5 drain the double-buffered accumulators
-// (2 x 256 TMEM columns) with tcgen05.ld and write the outputs.  Every mbarrier wait is
-// bounded: on expiry the kernel records LMOE timeout status, drains what it issued and
+// Weight-stationary tiles.  A tile is 256 weight rows (two MMA operands A0, A1 of M = 128
+// rows each) against up to kTokMax tokens (the MMA's N side, shared by both MMAs), with K
+// stepped 64 at a time (one 128-byte swizzle row of bf16):
+//   * GLU tiles: A0 = 128 gate rows, A1 = the 128 up rows of the same output features, so
+//     one TMEM lane holds both branches of a feature and the SiTU-GLU epilogue needs no
+//     exchange between warps;
+//   * store tiles: A0, A1 = two consecutive blocks of 128 output rows (A1 is skipped when
+//     it lies past the last output row);
+//   * an expert segment is covered by token tiles of kTokMax and one last tile rounded up
+//     to a multiple of 16 tokens, so each weight tile is streamed from HBM once per token
+//     tile (once per expert at prefill sizes), and each token row is re-read from L2 once
+//     per 128 output features.
+// Accumulators: TMEM holds 512 fp32 columns in two 256-column slots.  A tile of at most
+// 128 tokens takes one slot (A0 in its first 128 columns, A1 in the second), so two such
+// tiles double-buffer; a wider tile takes both slots (A0 in slot 0, A1 in slot 1).
+// Roles (384 threads): warp 0 streams weight tiles through a kWStages ring, warp 2 streams
+// token tiles through a kTStages ring (TMA, mbarrier completion), warp 1 owns TMEM and
+// issues tcgen05.mma (one thread), warps 4-11 drain the accumulators with tcgen05.ld (two
+// warps per TMEM lane quadrant, alternating 32-token chunks) and write the outputs.  The
+// expert tile schedule is copied into shared memory once per CTA.  Every mbarrier wait is
+// bounded: on expiry the kernel records the timeout status, drains what it issued and
 // returns.
 #include <cuda.h>
 
@@ -27,22 +35,31 @@
 namespace lmoe {
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kBK = 64;
-constexpr int kFeat = 128;
-constexpr int kTokMax = 256;
-constexpr int kTokBox = 16;
-constexpr int kAccCols = 256;
-constexpr int kStageW = kFeat * kBK * 2;     // 16 KB of weights per stage
-constexpr int kStageT = kTokMax * kBK * 2;   // 32 KB of tokens per stage
-constexpr int kThreads = 192;
-constexpr int kXStride = 17;                 // floats per exchange row (bank padding)
-constexpr int kXBuf = 2 * 64 * kXStride;     // floats per exchange buffer (gate + up halves)
-constexpr int kXchgBytes = 2 * kXBuf * 4;
-constexpr int kDenseGroup = 8;               // token tiles per raster group (dense GEMMs)
-constexpr int kNumBars = 2 * kStages + 5;
-constexpr int kSmemBytes = 1024 + kStages * (kStageW + kStageT) + kXchgBytes + kNumBars * 8 + 16;
+constexpr int kHalf = 128;                       // weight rows per MMA (M)
+constexpr int kTokMax = kTileM;                  // tokens per tile (MMA N), a multiple of 16
+constexpr int kTokBox = 16;                      // token rows per TMA box
+constexpr int kHalfBytes = kHalf * kBK * 2;      // 16 KB
+constexpr int kWStageBytes = 2 * kHalfBytes;     // 32 KB of weights per stage
+constexpr int kTStageBytes = kTokMax * kBK * 2;  // token rows per stage
+constexpr int kWStages = 5;
+constexpr int kTStages = 2;
+constexpr int kSlotCols = 256;
+constexpr int kEpiWarps = 8;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kThreads = 128 + kEpiThreads;
+constexpr int kSchedMax = 1024;                  // schedule entries kept in shared memory
+constexpr int kDenseGroup = 8;                   // token tiles per raster group (dense GEMMs)
+// barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
+constexpr int kNumBars = 2 * kWStages + 2 * kTStages + 4 + 1;
+constexpr int kOffT = kWStages * kWStageBytes;
+constexpr int kOffSched = kOffT + kTStages * kTStageBytes;
+constexpr int kOffBars = kOffSched + 2 * kSchedMax * 4;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = 1024 + kOffMisc + 16;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
+static_assert(kTokMax % 16 == 0 && kTokMax <= 256, "MMA N limit");
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 
 struct TcMaps {
   CUtensorMap w[kMaxKSeg];  // weight (MMA A) maps, one per K segment; GLU: w[0] = gate
@@ -56,12 +73,13 @@ struct TcParams {
   int seg_row0[kMaxKSeg];
   int w_group_rows;         // weight rows per group (routed experts), 0 for dense
   int n_feat;               // output features
-  int n_fb;                 // feature blocks (128 rows, or 64 outputs for GLU)
+  int n_fb;                 // feature blocks (256 output rows, or 128 GLU outputs)
   int kblocks;              // K / 64
   int bt;                   // dense: tokens
+  int tok_tile;             // dense: tokens per tile (<= kTokMax, multiple of 16)
   const int32_t* seg_off;   // grouped: [G + 1] token segments
-  const int32_t* mtile_off; // grouped: [G + 1] prefix of 256-token tiles
-  int G;
+  const int32_t* mtile_off; // grouped: [G + 1] prefix of kTokMax-token tiles
+  int G;                    // grouped: number of groups, 0 for dense
   void* out;
   long long ldo;
   float* out_t;
@@ -140,9 +158,9 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       : "memory");
 }
 
-// 32 lanes x 32 consecutive fp32 columns of TMEM (this warp's lane quadrant).
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
-  uint32_t r[32];
+// 32 lanes x 32 consecutive fp32 columns of TMEM (this warp's lane quadrant); the caller
+// waits with tmem_wait_ld() before reading the registers.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -151,10 +169,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes
 // in 8-row (1024-byte) groups; start address advanced by 32 bytes per K step of 16.
@@ -167,9 +183,6 @@ __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 // Barrier over the epilogue warps that also ORs a flag across them.
 __device__ __forceinline__ bool named_sync_or(int id, int n, bool flag) {
   uint32_t res;
@@ -188,42 +201,57 @@ struct Tile {
 };
 
 __device__ __forceinline__ int num_tiles(const TcParams& p) {
-  if (p.seg_off) return p.mtile_off[p.G] * p.n_fb;
-  return ((p.bt + kTokMax - 1) / kTokMax) * p.n_fb;
+  if (p.G > 0) return p.mtile_off[p.G] * p.n_fb;
+  return ((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb;
 }
 
-// Grouped: tiles ordered (expert, feature block, token tile) so the CTAs working at the
-// same time share weight tiles and token rows in L2.  Dense: token tiles in groups of
+// Grouped: tiles ordered (expert, feature block, token tile), so the CTAs working at the
+// same time share weight tiles and token rows in L2; seg/mt are the expert segment and
+// tile prefixes (shared memory when they fit).  Dense: token tiles in groups of
 // kDenseGroup, feature blocks inside a group.
-__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, const int32_t* seg, const int32_t* mt, int t) {
   Tile r;
-  if (p.seg_off) {
+  if (p.G > 0) {
     const int q = t / p.n_fb;
-    int lo = 0, hi = p.G;
+    int lo = 0, hi = p.G;                        // largest g with mt[g] <= q
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (p.mtile_off[mid] <= q) lo = mid; else hi = mid;
+      if (mt[mid] <= q) lo = mid; else hi = mid;
     }
-    const int m0 = p.mtile_off[lo];
-    const int nt = p.mtile_off[lo + 1] - m0;
+    const int m0 = mt[lo];
+    const int nt = mt[lo + 1] - m0;
     const int local = t - m0 * p.n_fb;
     r.g = lo;
     r.fb = local / nt;
     const int tb = local - r.fb * nt;
-    r.tok0 = p.seg_off[lo] + tb * kTokMax;
-    r.ntok = min(kTokMax, p.seg_off[lo + 1] - r.tok0);
+    r.tok0 = seg[lo] + tb * kTokMax;
+    r.ntok = min(kTokMax, seg[lo + 1] - r.tok0);
   } else {
-    const int nt = (p.bt + kTokMax - 1) / kTokMax;
+    const int nt = (p.bt + p.tok_tile - 1) / p.tok_tile;
     const int grp = t / (kDenseGroup * p.n_fb);
     const int in = t - grp * kDenseGroup * p.n_fb;
     const int gcnt = min(kDenseGroup, nt - grp * kDenseGroup);
     r.g = 0;
     r.fb = in / gcnt;
     const int tb = grp * kDenseGroup + (in - r.fb * gcnt);
-    r.tok0 = tb * kTokMax;
-    r.ntok = min(kTokMax, p.bt - r.tok0);
+    r.tok0 = tb * p.tok_tile;
+    r.ntok = min(p.tok_tile, p.bt - r.tok0);
   }
   return r;
+}
+
+// Weight operands of a tile: GLU always two (gate, up); store / router one or two blocks
+// of 128 output rows.
+template <int EPI>
+__device__ __forceinline__ int tile_halves(const TcParams& p, const Tile& tl) {
+  if (EPI == kEpiGlu) return 2;
+  return (p.n_feat - tl.fb * 2 * kHalf > kHalf) ? 2 : 1;
+}
+
+// TMEM columns of the two accumulators of a tile: narrow tiles (<= 128 tokens) use slot s,
+// wide ones both slots.
+__device__ __forceinline__ uint32_t acc_col(bool wide, int slot, int h) {
+  return wide ? (uint32_t)(h * kSlotCols) : (uint32_t)(slot * kSlotCols + h * kHalf);
 }
 
 // ------------------------------------------------------------------ the kernel
@@ -235,115 +263,174 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
   const uint32_t wbase = base;
-  const uint32_t tbase = base + kStages * kStageW;
-  float* xchg = reinterpret_cast<float*>(sbase + kStages * (kStageW + kStageT));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + kStages * (kStageW + kStageT) + kXchgBytes);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  const uint32_t tbase = base + kOffT;
+  int32_t* s_seg = reinterpret_cast<int32_t*>(sbase + kOffSched);
+  int32_t* s_mt = s_seg + kSchedMax;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + kOffBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
+  auto wempty_bar = [&](int s) { return bar0 + 8u * (kWStages + s); };
+  auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * kWStages + s); };
+  auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * kWStages + kTStages + s); };
+  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * kWStages + 2 * kTStages + a); };
+  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * kWStages + 2 * kTStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kWStages + 2 * kTStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) { mbar_init(full_bar(s), 1); mbar_init(empty_bar(s), 1); }
-    for (int a = 0; a < 2; ++a) { mbar_init(tfull_bar(a), 1); mbar_init(tempty_bar(a), 128); }
+    for (int s = 0; s < kWStages; ++s) { mbar_init(wfull_bar(s), 1); mbar_init(wempty_bar(s), 1); }
+    for (int s = 0; s < kTStages; ++s) { mbar_init(tfull_bar(s), 1); mbar_init(tempty_bar(s), 1); }
+    for (int a = 0; a < 2; ++a) { mbar_init(afull_bar(a), 1); mbar_init(aempty_bar(a), kEpiWarps); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  const bool sched_smem = p.G > 0 && p.G < kSchedMax;
+  if (sched_smem) {
+    for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
+      s_seg[i] = p.seg_off[i];
+      s_mt[i] = p.mtile_off[i];
+    }
+  }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                 "r"(2 * kAccCols));
+                 "r"(2 * kSlotCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int32_t* seg = sched_smem ? s_seg : p.seg_off;
+  const int32_t* mt = sched_smem ? s_mt : p.mtile_off;
   const int ntiles = num_tiles(p);
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t pending = 0;                       // stages with loads not yet re-acquired
-    uint32_t pend_parity = 0;
-    bool stop = false;
-    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
-      const Tile tl = decode_tile(p, t);
-      const int ntr = (tl.ntok + 15) & ~15;
-      const uint32_t bytes = kStageW + (uint32_t)ntr * (kBK * 2);
-      const int nbox = ntr / kTokBox;
-      for (int kb = 0; kb < p.kblocks; ++kb) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(empty_bar(stage), phase ^ 1u, abort_flag, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) { stop = true; break; }
-        pending &= ~(1u << stage);
-        if (lane == 0) mbar_expect_tx(full_bar(stage), bytes);
-        __syncwarp();
-        const uint32_t wdst = wbase + stage * kStageW, tdst = tbase + stage * kStageT;
-        const int k = kb * kBK;
-        if (lane == 0) {
+    // ---------------------------------------------------------------- weight producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, pending = 0, pend_parity = 0;
+      bool stop = false;
+      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+        const Tile tl = decode_tile(p, seg, mt, t);
+        const int nh = tile_halves<EPI>(p, tl);
+        for (int kb = 0; kb < p.kblocks; ++kb) {
+          if (!mbar_wait(wempty_bar(stage), phase ^ 1u, abort_flag, p.status)) { stop = true; break; }
+          pending &= ~(1u << stage);
+          mbar_expect_tx(wfull_bar(stage), (uint32_t)(nh * kHalfBytes));
+          const uint32_t dst = wbase + stage * kWStageBytes;
+          const int k = kb * kBK;
           if (EPI == kEpiGlu) {
-            const int row = tl.g * p.w_group_rows + tl.fb * 64;
-            tma_load_2d(wdst, &maps.w[0], k, row, full_bar(stage));
-            tma_load_2d(wdst + 64 * kBK * 2, &maps.wup, k, row, full_bar(stage));
+            const int row = tl.g * p.w_group_rows + tl.fb * kHalf;
+            tma_load_2d(dst, &maps.w[0], k, row, wfull_bar(stage));
+            tma_load_2d(dst + kHalfBytes, &maps.wup, k, row, wfull_bar(stage));
           } else {
             int s = 0;
 #pragma unroll
             for (int i = 1; i < kMaxKSeg; ++i)
               if (i < p.nseg && k >= p.seg_k0[i]) s = i;
-            const int row = p.seg_row0[s] + tl.g * p.w_group_rows + tl.fb * kFeat;
-            tma_load_2d(wdst, &maps.w[s], k - p.seg_k0[s], row, full_bar(stage));
+            const int row = p.seg_row0[s] + tl.g * p.w_group_rows + tl.fb * 2 * kHalf;
+            tma_load_2d(dst, &maps.w[s], k - p.seg_k0[s], row, wfull_bar(stage));
+            if (nh == 2) tma_load_2d(dst + kHalfBytes, &maps.w[s], k - p.seg_k0[s], row + kHalf, wfull_bar(stage));
           }
+          pending |= 1u << stage;
+          pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
         }
-        if (lane < nbox) tma_load_2d(tdst + lane * (kTokBox * kBK * 2), &maps.tok, k, tl.tok0 + lane * kTokBox,
-                                     full_bar(stage));
+      }
+      if (stop) {
+        // no copy may still be landing in shared memory when the block exits
+        for (int s = 0; s < kWStages; ++s)
+          if (pending & (1u << s)) mbar_wait(wfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, false);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- token producer
+    int stage = 0;
+    uint32_t phase = 0, pending = 0, pend_parity = 0;
+    bool stop = false;
+    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
+      const Tile tl = decode_tile(p, seg, mt, t);
+      const int ntr = (tl.ntok + 15) & ~15;
+      const int nbox = ntr / kTokBox;
+      for (int kb = 0; kb < p.kblocks; ++kb) {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(tempty_bar(stage), phase ^ 1u, abort_flag, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) { stop = true; break; }
+        pending &= ~(1u << stage);
+        if (lane == 0) mbar_expect_tx(tfull_bar(stage), (uint32_t)ntr * (kBK * 2));
+        __syncwarp();
+        const uint32_t dst = tbase + stage * kTStageBytes;
+        if (lane < nbox)
+          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, kb * kBK, tl.tok0 + lane * kTokBox, tfull_bar(stage));
         pending |= 1u << stage;
         pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kStages) { stage = 0; phase ^= 1u; }
+        if (++stage == kTStages) { stage = 0; phase ^= 1u; }
       }
     }
     if (stop && lane == 0) {
-      // no copy may still be landing in shared memory when the block exits
-      for (int s = 0; s < kStages; ++s)
-        if (pending & (1u << s)) mbar_wait(full_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, false);
+      for (int s = 0; s < kTStages; ++s)
+        if (pending & (1u << s)) mbar_wait(tfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, false);
     }
+    __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      int ws = 0, ts = 0, slot = 0;
+      uint32_t wph = 0, tph = 0;
+      uint32_t aph[2] = {0u, 0u};
       bool stop = false, issued = false;
       for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
-        const Tile tl = decode_tile(p, t);
+        const Tile tl = decode_tile(p, seg, mt, t);
         const int ntr = (tl.ntok + 15) & ~15;
-        const uint32_t idesc = idesc_bf16(kFeat, ntr);
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status)) { stop = true; break; }
+        const bool wide = ntr > kHalf;
+        const int nh = tile_halves<EPI>(p, tl);
+        const uint32_t idesc = idesc_bf16(kHalf, ntr);
+        if (wide) {
+          if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status) ||
+              !mbar_wait(aempty_bar(1), aph[1] ^ 1u, abort_flag, p.status)) { stop = true; break; }
+        } else {
+          if (!mbar_wait(aempty_bar(slot), aph[slot] ^ 1u, abort_flag, p.status)) { stop = true; break; }
+        }
         tc_fence_after();
-        const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+        const uint32_t d0 = tmem_base + acc_col(wide, slot, 0);
+        const uint32_t d1 = tmem_base + acc_col(wide, slot, 1);
         for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort_flag, p.status)) { stop = true; break; }
+          if (!mbar_wait(wfull_bar(ws), wph, abort_flag, p.status) ||
+              !mbar_wait(tfull_bar(ts), tph, abort_flag, p.status)) { stop = true; break; }
           tc_fence_after();
-          const uint64_t ad = smem_desc(wbase + stage * kStageW);
-          const uint64_t bd = smem_desc(tbase + stage * kStageT);
+          const uint64_t ad = smem_desc(wbase + ws * kWStageBytes);
+          const uint64_t bd = smem_desc(tbase + ts * kTStageBytes);
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)
-            tc_mma(d, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+            tc_mma(d0, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+          if (nh == 2) {
+            const uint64_t ad1 = ad + (uint64_t)(kHalfBytes >> 4);
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j)
+              tc_mma(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+          }
           issued = true;
-          tc_commit(empty_bar(stage));
-          if (++stage == kStages) { stage = 0; phase ^= 1u; }
+          tc_commit(wempty_bar(ws));
+          tc_commit(tempty_bar(ts));
+          if (++ws == kWStages) { ws = 0; wph ^= 1u; }
+          if (++ts == kTStages) { ts = 0; tph ^= 1u; }
         }
         if (stop) break;
-        tc_commit(tfull_bar(acc));
-        if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        if (wide) {
+          tc_commit(afull_bar(0));
+          tc_commit(afull_bar(1));
+          aph[0] ^= 1u;
+          aph[1] ^= 1u;
+        } else {
+          tc_commit(afull_bar(slot));
+          aph[slot] ^= 1u;
+          slot ^= 1;
+        }
       }
       if (stop && issued) {
         tc_commit(drain_bar);
@@ -351,81 +438,91 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       }
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    int chunk_ctr = 0;
+    const int sub = (warp - 4) >> 2;        // which 32-token chunks: sub, sub + 2, ...
+    const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+    int slot = 0;
+    uint32_t aph[2] = {0u, 0u};
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile tl = decode_tile(p, t);
-      const bool ok = mbar_wait(tfull_bar(acc), acc_phase, abort_flag, p.status);
-      if (named_sync_or(2, 128, !ok || *abort_flag)) break;
+      const Tile tl = decode_tile(p, seg, mt, t);
+      const int ntr = (tl.ntok + 15) & ~15;
+      const bool wide = ntr > kHalf;
+      const int nh = tile_halves<EPI>(p, tl);
+      bool ok;
+      if (wide) ok = mbar_wait(afull_bar(0), aph[0], abort_flag, p.status) &&
+                     mbar_wait(afull_bar(1), aph[1], abort_flag, p.status);
+      else ok = mbar_wait(afull_bar(slot), aph[slot], abort_flag, p.status);
+      if (named_sync_or(1, kEpiThreads, !ok || *abort_flag)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kAccCols);
-      const int nchunks = (tl.ntok + 31) / 32;
+      const uint32_t c0 = lane_base + acc_col(wide, slot, 0);
+      const uint32_t c1 = lane_base + acc_col(wide, slot, 1);
+      const int nchunks = (tl.ntok + 31) >> 5;
       if (EPI == kEpiGlu) {
-        const int r64 = (q & 1) * 32 + lane;       // row inside the gate (q 0,1) or up (q 2,3) half
-        const int fout = tl.fb * 64 + r64;
-        bf16* out = static_cast<bf16*>(p.out);
-        for (int c = 0; c < nchunks; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          float* xg = xchg + (chunk_ctr & 1) * kXBuf;
-          float* xu = xg + 64 * kXStride;
-          if (q < 2) {
+        const int fout = tl.fb * kHalf + q * 32 + lane;
+        const bool fok = fout < p.n_feat;
+        bf16* out = static_cast<bf16*>(p.out) + fout;
+        for (int c = sub; c < nchunks; c += 2) {
+          uint32_t g[32], u[32];
+          tmem_ld32(c0 + c * 32, g);
+          tmem_ld32(c1 + c * 32, u);
+          tmem_wait_ld();
+          if (!fok) continue;
+          const int nj = min(32, tl.ntok - c * 32);
+          bf16* o = out + (long long)(tl.tok0 + c * 32) * p.ldo;
 #pragma unroll
-            for (int j = 0; j < 16; ++j) xg[r64 * kXStride + j] = v[16 + j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) xu[r64 * kXStride + j] = v[j];
-          }
-          named_sync(1, 128);
-          const int jb = c * 32 + (q < 2 ? 0 : 16);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float gv = q < 2 ? v[j] : xg[r64 * kXStride + j];
-            const float uv = q < 2 ? xu[r64 * kXStride + j] : v[16 + j];
-            const int tok = jb + j;
-            if (tok < tl.ntok && fout < p.n_feat)
-              out[(long long)(tl.tok0 + tok) * p.ldo + fout] = __float2bfloat16_rn(situ_glu(gv, uv, p.beta, p.beta_u));
-          }
-          ++chunk_ctr;
+          for (int j = 0; j < 32; ++j)
+            if (j < nj)
+              o[(long long)j * p.ldo] =
+                  __float2bfloat16_rn(situ_glu(__uint_as_float(g[j]), __uint_as_float(u[j]), p.beta, p.beta_u));
         }
       } else {
-        const int fout = tl.fb * kFeat + q * 32 + lane;
-        const bool fok = fout < p.n_feat;
-        const float bias = (EPI == kEpiRouter && fok && p.bias) ? p.bias[fout] : 0.f;
-        for (int c = 0; c < nchunks; ++c) {
-          float v[32];
-          tmem_ld32(taddr + c * 32, v);
-          if (!fok) continue;
+        const int f0 = tl.fb * 2 * kHalf + q * 32 + lane;
+        for (int c = sub; c < nchunks; c += 2) {
+          const int nj = min(32, tl.ntok - c * 32);
+          for (int h = 0; h < nh; ++h) {
+            uint32_t v[32];
+            tmem_ld32((h ? c1 : c0) + c * 32, v);
+            tmem_wait_ld();
+            const int fout = f0 + h * kHalf;
+            if (fout >= p.n_feat) continue;
+            const long long row0 = tl.tok0 + c * 32;
+            if (EPI == kEpiStore) {
+              bf16* o = static_cast<bf16*>(p.out) + row0 * p.ldo + fout;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int tok = c * 32 + j;
-            if (tok < tl.ntok) {
-              const long long row = tl.tok0 + tok;
-              if (EPI == kEpiStore) {
-                static_cast<bf16*>(p.out)[row * p.ldo + fout] = __float2bfloat16_rn(v[j]);
-              } else {
-                const float val = v[j] + bias;
-                static_cast<float*>(p.out)[row * p.ldo + fout] = val;
-                p.out_t[(long long)fout * p.ldt + row] = val;
-              }
+              for (int j = 0; j < 32; ++j)
+                if (j < nj) o[(long long)j * p.ldo] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            } else {
+              const float bias = p.bias ? p.bias[fout] : 0.f;
+              float* o = static_cast<float*>(p.out) + row0 * p.ldo + fout;
+              float* ot = p.out_t + (long long)fout * p.ldt + row0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nj) {
+                  const float val = __uint_as_float(v[j]) + bias;
+                  o[(long long)j * p.ldo] = val;
+                  ot[j] = val;
+                }
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
-      if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+      __syncwarp();
+      if (lane == 0) {
+        if (wide) { mbar_arrive(aempty_bar(0)); mbar_arrive(aempty_bar(1)); }
+        else mbar_arrive(aempty_bar(slot));
+      }
+      if (wide) { aph[0] ^= 1u; aph[1] ^= 1u; }
+      else { aph[slot] ^= 1u; slot ^= 1; }
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols));
+  if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kSlotCols));
 }
 
 // Routed-expert token rows in slot order: zp[slot] = z[perm[slot]] (16-byte vectors).
@@ -497,11 +594,11 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int ma
   const long long E = c.n_experts, d = c.d, L = c.latent, I = c.expert_inter, S = c.n_shared, Is = c.shared_inter;
   const long long ldc = L + S * Is;
   const long long slots = (long long)max_bt * c.top_k;
-  bool ok = make_map(&pl->m_router, w->w_router, E, d, d, kFeat) && make_map(&pl->m_down, w->w_down, L, d, d, kFeat) &&
-            make_map(&pl->m_gate, w->exp_gate, E * I, L, L, 64) && make_map(&pl->m_up, w->exp_up, E * I, L, L, 64) &&
-            make_map(&pl->m_edown, w->exp_down, E * L, I, I, kFeat) &&
-            make_map(&pl->m_shg, w->sh_gate, S * Is, d, d, 64) && make_map(&pl->m_shu, w->sh_up, S * Is, d, d, 64) &&
-            make_map(&pl->m_wup, w->w_up, d, L, L, kFeat) && make_map(&pl->m_shd, w->sh_down, S * d, Is, Is, kFeat) &&
+  bool ok = make_map(&pl->m_router, w->w_router, E, d, d, kHalf) && make_map(&pl->m_down, w->w_down, L, d, d, kHalf) &&
+            make_map(&pl->m_gate, w->exp_gate, E * I, L, L, kHalf) && make_map(&pl->m_up, w->exp_up, E * I, L, L, kHalf) &&
+            make_map(&pl->m_edown, w->exp_down, E * L, I, I, kHalf) &&
+            make_map(&pl->m_shg, w->sh_gate, S * Is, d, d, kHalf) && make_map(&pl->m_shu, w->sh_up, S * Is, d, d, kHalf) &&
+            make_map(&pl->m_wup, w->w_up, d, L, L, kHalf) && make_map(&pl->m_shd, w->sh_down, S * d, Is, Is, kHalf) &&
             make_map(&pl->m_zp, buf.zp, slots, L, L, kTokBox) && make_map(&pl->m_h, buf.h, slots, I, I, kTokBox) &&
             make_map(&pl->m_cat, buf.cat, max_bt, ldc, ldc, kTokBox);
   if (!ok) {
@@ -542,6 +639,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   p.beta = a.beta;
   p.beta_u = a.beta_u;
   p.status = pl->buf.status;
+  p.tok_tile = kTokMax;
   int epi = a.epi;
   bool ok = true;
   switch (a.op) {
@@ -602,10 +700,10 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
       return cudaErrorInvalidValue;
   }
   if (!ok) return cudaErrorInvalidValue;
-  p.n_fb = epi == kEpiGlu ? (a.N + 63) / 64 : (a.N + kFeat - 1) / kFeat;
+  p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
   int grid = pl->sm_count;
-  if (!p.seg_off) {
-    const long long tiles = (long long)((p.bt + kTokMax - 1) / kTokMax) * p.n_fb;
+  if (p.G == 0) {
+    const long long tiles = (long long)((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb;
     if (tiles < grid) grid = (int)tiles;
   }
   if (grid <= 0) return cudaSuccess;
