@@ -17,10 +17,13 @@
 // Accumulators: TMEM holds 512 fp32 columns in two 256-column slots.  A tile of at most
 // 128 tokens takes one slot (A0 in its first 128 columns, A1 in the second), so two such
 // tiles double-buffer; a wider tile takes both slots (A0 in slot 0, A1 in slot 1).
-// Roles (384 threads): warp 0 streams weight tiles through a kWStages ring, warp 2 streams
+// Roles (512 threads): warp 0 streams weight tiles through a kWStages ring, warp 2 streams
 // token tiles through a kTStages ring (TMA, mbarrier completion), warp 1 owns TMEM and
-// issues tcgen05.mma (one thread), warps 4-11 drain the accumulators with tcgen05.ld (two
-// warps per TMEM lane quadrant, alternating 32-token chunks) and write the outputs.  The
+// issues tcgen05.mma (one thread), warps 4-15 drain the accumulators with tcgen05.ld (three
+// warps per TMEM lane quadrant, taking every third 32-token chunk) and write the outputs.
+// While a wide tile drains, the next one cannot start, so the SiTU-GLU epilogue uses the
+// hardware tanh approximation (relative error about 2^-11, below the bf16 rounding of its
+// output) to keep that gap short.  The
 // expert tile schedule is copied into shared memory once per CTA.  Every mbarrier wait is
 // bounded: on expiry the kernel records the timeout status, drains what it issued and
 // returns.
@@ -42,12 +45,13 @@ constexpr int kTokBox = 16;                      // token rows per TMA box
 constexpr int kHalfBytes = kHalf * kBK * 2;      // 16 KB
 constexpr int kWStageBytes = 2 * kHalfBytes;     // 32 KB of weights per stage
 constexpr int kTStageBytes = kTokMax * kBK * 2;  // token rows per stage
-constexpr int kWStages = 5;
-constexpr int kTStages = 2;
+constexpr int kWStages = 4;
+constexpr int kTStages = 3;
 constexpr int kSlotCols = 256;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 12;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 128 + kEpiThreads;
+constexpr int kMaxChunks = (kTokMax / 32 + 2) / 3;   // 32-token chunks per epilogue warp
 constexpr int kSchedMax = 1024;                  // schedule entries kept in shared memory
 constexpr int kDenseGroup = 8;                   // token tiles per raster group (dense GEMMs)
 // barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
@@ -86,6 +90,7 @@ struct TcParams {
   long long ldt;
   const float* bias;
   float beta, beta_u;
+  float inv_beta, inv_beta_u;
   uint32_t* status;
 };
 
@@ -138,11 +143,26 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   }
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// 2-D TMA tile load into shared memory, completing on an mbarrier, with an L2 policy.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                            uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
+}
+// L2 policies: weights are streamed once (evict first); token rows are re-read by every
+// feature block of their tile (evict last).
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -181,6 +201,27 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 accumulator.
 __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+// tanh by the MUFU hardware approximation (PTX tanh.approx.f32).
+__device__ __forceinline__ float tanh_hw(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+// SiTU-GLU from three hardware tanh: g' = beta tanh(g / beta), u' = beta_u tanh(u / beta_u),
+// act = g' sigmoid(g') u' with sigmoid(v) = (1 + tanh(v / 2)) / 2.
+template <typename P>
+__device__ __forceinline__ float situ_glu_fast(float g, float u, const P& p) {
+  const float gp = p.beta * tanh_hw(g * p.inv_beta);
+  const float up = p.beta_u * tanh_hw(u * p.inv_beta_u);
+  const float sg = fmaf(0.5f, tanh_hw(0.5f * gp), 0.5f);
+  return gp * sg * up;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
 }
 
 // Barrier over the epilogue warps that also ORs a flag across them.
@@ -238,6 +279,15 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int32_t* se
     r.ntok = min(p.tok_tile, p.bt - r.tok0);
   }
   return r;
+}
+
+// K order of a tile: the feature blocks of one token tile run on neighbouring CTAs at the
+// same time and read the same token rows, so each starts its K loop at a different
+// offset (evenly spread); every token k-block is then fetched from DRAM by one CTA and
+// found in L2 by the others.  The order is fixed per tile, so results are deterministic.
+__device__ __forceinline__ int k_rot(const TcParams& p, const Tile& tl, int kb) {
+  int k = kb + (int)(((long long)tl.fb * p.kblocks) / p.n_fb);
+  return k >= p.kblocks ? k - p.kblocks : k;
 }
 
 // Weight operands of a tile: GLU always two (gate, up); store / router one or two blocks
@@ -309,7 +359,25 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
 
   if (warp == 0) {
     // ---------------------------------------------------------------- weight producer
+    // Weight operand h of k-block kb of a tile: tensor map and coordinates.
+    auto w_src = [&](const Tile& tl, int kb, int h, const CUtensorMap*& m, int& x, int& y) {
+      const int k = kb * kBK;
+      if (EPI == kEpiGlu) {
+        m = h ? &maps.wup : &maps.w[0];
+        x = k;
+        y = tl.g * p.w_group_rows + tl.fb * kHalf;
+      } else {
+        int s = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxKSeg; ++i)
+          if (i < p.nseg && k >= p.seg_k0[i]) s = i;
+        m = &maps.w[s];
+        x = k - p.seg_k0[s];
+        y = p.seg_row0[s] + tl.g * p.w_group_rows + tl.fb * 2 * kHalf + h * kHalf;
+      }
+    };
     if (lane == 0) {
+      const uint64_t wpol = policy_evict_first();
       int stage = 0;
       uint32_t phase = 0, pending = 0, pend_parity = 0;
       bool stop = false;
@@ -321,19 +389,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           pending &= ~(1u << stage);
           mbar_expect_tx(wfull_bar(stage), (uint32_t)(nh * kHalfBytes));
           const uint32_t dst = wbase + stage * kWStageBytes;
-          const int k = kb * kBK;
-          if (EPI == kEpiGlu) {
-            const int row = tl.g * p.w_group_rows + tl.fb * kHalf;
-            tma_load_2d(dst, &maps.w[0], k, row, wfull_bar(stage));
-            tma_load_2d(dst + kHalfBytes, &maps.wup, k, row, wfull_bar(stage));
-          } else {
-            int s = 0;
-#pragma unroll
-            for (int i = 1; i < kMaxKSeg; ++i)
-              if (i < p.nseg && k >= p.seg_k0[i]) s = i;
-            const int row = p.seg_row0[s] + tl.g * p.w_group_rows + tl.fb * 2 * kHalf;
-            tma_load_2d(dst, &maps.w[s], k - p.seg_k0[s], row, wfull_bar(stage));
-            if (nh == 2) tma_load_2d(dst + kHalfBytes, &maps.w[s], k - p.seg_k0[s], row + kHalf, wfull_bar(stage));
+          for (int h = 0; h < nh; ++h) {
+            const CUtensorMap* m;
+            int x, y;
+            w_src(tl, k_rot(p, tl, kb), h, m, x, y);
+            tma_load_2d(dst + h * kHalfBytes, m, x, y, wfull_bar(stage), wpol);
           }
           pending |= 1u << stage;
           pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
@@ -349,6 +409,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     __syncwarp();
   } else if (warp == 2) {
     // ---------------------------------------------------------------- token producer
+    const uint64_t tpol = policy_evict_last();
     int stage = 0;
     uint32_t phase = 0, pending = 0, pend_parity = 0;
     bool stop = false;
@@ -366,7 +427,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         __syncwarp();
         const uint32_t dst = tbase + stage * kTStageBytes;
         if (lane < nbox)
-          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, kb * kBK, tl.tok0 + lane * kTokBox, tfull_bar(stage));
+          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, k_rot(p, tl, kb) * kBK, tl.tok0 + lane * kTokBox,
+                      tfull_bar(stage), tpol);
         pending |= 1u << stage;
         pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == kTStages) { stage = 0; phase ^= 1u; }
@@ -441,7 +503,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int q = warp & 3;                 // TMEM lane quadrant of this warp
-    const int sub = (warp - 4) >> 2;        // which 32-token chunks: sub, sub + 2, ...
+    const int sub = (warp - 4) >> 2;        // which 32-token chunks: sub, sub + 3, ...
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     int slot = 0;
     uint32_t aph[2] = {0u, 0u};
@@ -459,27 +521,46 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const uint32_t c0 = lane_base + acc_col(wide, slot, 0);
       const uint32_t c1 = lane_base + acc_col(wide, slot, 1);
       const int nchunks = (tl.ntok + 31) >> 5;
+      // Results of this warp's chunks (<= kMaxChunks), packed bf16 pairs of consecutive
+      // tokens; TMEM is released before they are written out.
+      uint32_t res[kMaxChunks][2][16];
       if (EPI == kEpiGlu) {
-        const int fout = tl.fb * kHalf + q * 32 + lane;
-        const bool fok = fout < p.n_feat;
-        bf16* out = static_cast<bf16*>(p.out) + fout;
-        for (int c = sub; c < nchunks; c += 2) {
-          uint32_t g[32], u[32];
-          tmem_ld32(c0 + c * 32, g);
-          tmem_ld32(c1 + c * 32, u);
-          tmem_wait_ld();
-          if (!fok) continue;
-          const int nj = min(32, tl.ntok - c * 32);
-          bf16* o = out + (long long)(tl.tok0 + c * 32) * p.ldo;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nj)
-              o[(long long)j * p.ldo] =
-                  __float2bfloat16_rn(situ_glu(__uint_as_float(g[j]), __uint_as_float(u[j]), p.beta, p.beta_u));
+        for (int ci = 0; ci < kMaxChunks; ++ci) {
+          const int c = sub + 3 * ci;
+          if (c < nchunks) {
+            uint32_t g[32], u[32];
+            tmem_ld32(c0 + c * 32, g);
+            tmem_ld32(c1 + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              res[ci][0][j] = pack_bf16x2(situ_glu_fast(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]), p),
+                                          situ_glu_fast(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]), p));
+          }
+        }
+      } else if (EPI == kEpiStore) {
+#pragma unroll
+        for (int ci = 0; ci < kMaxChunks; ++ci) {
+          const int c = sub + 3 * ci;
+          if (c < nchunks) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              if (h < nh) {
+                uint32_t v[32];
+                tmem_ld32((h ? c1 : c0) + c * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                  res[ci][h][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+              }
+            }
+          }
         }
       } else {
+        // router: fp32 logits and their transpose, written straight from TMEM
         const int f0 = tl.fb * 2 * kHalf + q * 32 + lane;
-        for (int c = sub; c < nchunks; c += 2) {
+        for (int c = sub; c < nchunks; c += 3) {
           const int nj = min(32, tl.ntok - c * 32);
           for (int h = 0; h < nh; ++h) {
             uint32_t v[32];
@@ -488,23 +569,16 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             const int fout = f0 + h * kHalf;
             if (fout >= p.n_feat) continue;
             const long long row0 = tl.tok0 + c * 32;
-            if (EPI == kEpiStore) {
-              bf16* o = static_cast<bf16*>(p.out) + row0 * p.ldo + fout;
+            const float bias = p.bias ? p.bias[fout] : 0.f;
+            float* o = static_cast<float*>(p.out) + row0 * p.ldo + fout;
+            float* ot = p.out_t + (long long)fout * p.ldt + row0;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nj) o[(long long)j * p.ldo] = __float2bfloat16_rn(__uint_as_float(v[j]));
-            } else {
-              const float bias = p.bias ? p.bias[fout] : 0.f;
-              float* o = static_cast<float*>(p.out) + row0 * p.ldo + fout;
-              float* ot = p.out_t + (long long)fout * p.ldt + row0;
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nj) {
-                  const float val = __uint_as_float(v[j]) + bias;
-                  o[(long long)j * p.ldo] = val;
-                  ot[j] = val;
-                }
-            }
+            for (int j = 0; j < 32; ++j)
+              if (j < nj) {
+                const float val = __uint_as_float(v[j]) + bias;
+                o[(long long)j * p.ldo] = val;
+                ot[j] = val;
+              }
           }
         }
       }
@@ -513,6 +587,27 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       if (lane == 0) {
         if (wide) { mbar_arrive(aempty_bar(0)); mbar_arrive(aempty_bar(1)); }
         else mbar_arrive(aempty_bar(slot));
+      }
+      if (EPI != kEpiRouter) {
+        const int fbase = EPI == kEpiGlu ? tl.fb * kHalf + q * 32 + lane : tl.fb * 2 * kHalf + q * 32 + lane;
+#pragma unroll
+        for (int ci = 0; ci < kMaxChunks; ++ci) {
+          const int c = sub + 3 * ci;
+          if (c >= nchunks) continue;
+          const int nj = min(32, tl.ntok - c * 32);
+#pragma unroll
+          for (int h = 0; h < (EPI == kEpiGlu ? 1 : 2); ++h) {
+            const int fout = fbase + h * kHalf;
+            if (h >= nh || fout >= p.n_feat) continue;
+            bf16* o = static_cast<bf16*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nj) {
+                const uint32_t w2 = res[ci][h][j >> 1];
+                o[(long long)j * p.ldo] = __ushort_as_bfloat16((unsigned short)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu)));
+              }
+          }
+        }
       }
       if (wide) { aph[0] ^= 1u; aph[1] ^= 1u; }
       else { aph[slot] ^= 1u; slot ^= 1; }
@@ -638,6 +733,8 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   p.ldo = a.ldo;
   p.beta = a.beta;
   p.beta_u = a.beta_u;
+  p.inv_beta = 1.0f / a.beta;
+  p.inv_beta_u = 1.0f / a.beta_u;
   p.status = pl->buf.status;
   p.tok_tile = kTokMax;
   int epi = a.epi;

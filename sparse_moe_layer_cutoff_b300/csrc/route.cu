@@ -101,11 +101,26 @@ qb_cutoff_kernel(const float* __restrict__ logits_t, int bt, int n_experts, int 
 }
 
 // ------------------------------------------------------------------------------------
-// Top-K per token: one warp per token.  Keys s - alpha (fp64) live in shared memory; each
-// lane keeps the best of its own experts (e = lane + 32 i) and the warp picks the best of
-// the lane bests K times.  Order: key descending, then expert index ascending.
+// Top-K per token: one warp per token, exact in fp64 but with fp64 work only where it can
+// change the answer (the fp64 pipe of this GPU is narrow, so the bulk stays in fp32 and
+// integer arithmetic).
+//   1. fp32 keys k32[e] = 1 / (1 + expf(-l)) - (float)alpha[e] for every expert, kept as
+//      order-preserving uint32.  Against the fp64 key s - alpha the error is at most
+//      4.5e-7 (expf within 2 ulp; correctly rounded add, divide, conversion and subtract;
+//      keys lie in [-1, 1]); kKeyTol = 1e-6 bounds it.
+//   2. v = the K-th largest k32, built bit by bit from warp-wide counts (32 steps).
+//   3. Any expert with k32 < v - 2 kKeyTol has an fp64 key below the K-th largest fp64 key
+//      (K experts have fp64 keys >= v - kKeyTol), so it cannot be chosen: the candidates
+//      are the experts with k32 >= v - 2 kKeyTol (usually K or K+1 of them).
+//   4. fp64 keys for the candidates only; each candidate's rank among them (key
+//      descending, ties to the lower expert index) is its output slot if below K.  With
+//      more than 32 candidates (near-ties, K > 32) K rounds of warp argmax do the same.
+// Combine weights are the chosen fp64 scores over their sum (summed in k order).
 // ------------------------------------------------------------------------------------
-constexpr int kTopkWarps = 4;
+constexpr float kKeyTol = 1e-6f;
+constexpr double kTaken64 = -3.0;     // below every key (keys lie in [-1, 1])
+constexpr int kTopkMaxWarps = 8;
+constexpr size_t kTopkSmemCap = 96 * 1024;
 
 __device__ __forceinline__ bool topk_better(bool v1, double k1, int e1, bool v2, double k2, int e2) {
   if (v1 != v2) return v1;
@@ -113,56 +128,115 @@ __device__ __forceinline__ bool topk_better(bool v1, double k1, int e1, bool v2,
   return k1 > k2 || (k1 == k2 && e1 < e2);
 }
 
-__global__ void __launch_bounds__(kTopkWarps * 32)
+// Warp argmax over lane-held (valid, key, index); ties to the lower index.  All lanes get
+// the winner.
+__device__ __forceinline__ void warp_best(bool& v, double& k, int& e) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const bool v2 = __shfl_xor_sync(0xffffffffu, v, o);
+    const double k2 = __shfl_xor_sync(0xffffffffu, k, o);
+    const int e2 = __shfl_xor_sync(0xffffffffu, e, o);
+    if (topk_better(v2, k2, e2, v, k, e)) { v = v2; k = k2; e = e2; }
+  }
+}
+
+__global__ void __launch_bounds__(kTopkMaxWarps * 32)
 topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, int bt,
             int n_experts, int top_k, int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
   extern __shared__ double smem_d[];
-  double* s_alpha = smem_d;                                        // [E]
+  const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  double* keys = smem_d + n_experts + (size_t)warp * n_experts;   // [E] per warp
-  double* chosen_s = smem_d + (size_t)(kTopkWarps + 1) * n_experts + warp * 64;  // [K<=64]
-  uint8_t* taken = reinterpret_cast<uint8_t*>(smem_d + (size_t)(kTopkWarps + 1) * n_experts +
-                                              kTopkWarps * 64) + (size_t)warp * n_experts;
+  const int E = n_experts;
+  double* s_alpha = smem_d;                                                       // [E]
+  double* ckey = smem_d + E + (size_t)warp * E;                                   // [E] candidate fp64 keys
+  double* chosen_s = smem_d + (size_t)(nwarps + 1) * E + (size_t)warp * kMaxTopK; // [K]
+  float* s_alpha32 = reinterpret_cast<float*>(smem_d + (size_t)(nwarps + 1) * E + (size_t)nwarps * kMaxTopK);
+  uint32_t* ku = reinterpret_cast<uint32_t*>(s_alpha32 + E) + (size_t)warp * 2 * E;   // [E] fp32 keys
+  int32_t* cid = reinterpret_cast<int32_t*>(ku + E);                              // [E] candidates
 
-  for (int e = threadIdx.x; e < n_experts; e += blockDim.x) s_alpha[e] = alpha[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const double a = alpha[e];
+    s_alpha[e] = a;
+    s_alpha32[e] = (float)a;
+  }
   __syncthreads();
 
-  for (int t = blockIdx.x * kTopkWarps + warp; t < bt; t += gridDim.x * kTopkWarps) {
-    const float* lrow = logits + (size_t)t * n_experts;
-    bool bv = false; double bk = 0.0; int be = 0;
-    for (int e = lane; e < n_experts; e += 32) {
-      double kv = sigmoid_f64((double)lrow[e]) - s_alpha[e];
-      keys[e] = kv;
-      taken[e] = 0;
-      if (!bv || kv > bk) { bv = true; bk = kv; be = e; }
+  for (int t = blockIdx.x * nwarps + warp; t < bt; t += gridDim.x * nwarps) {
+    const float* lrow = logits + (size_t)t * E;
+    // 1. fp32 keys
+    for (int e = lane; e < E; e += 32)
+      ku[e] = f32_to_key(1.0f / (1.0f + expf(-lrow[e])) - s_alpha32[e]);
+    __syncwarp();
+    // 2. the K-th largest key: the largest v with at least K keys >= v
+    uint32_t v = 0;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = v | (1u << bit);
+      uint32_t c = 0;
+      for (int e = lane; e < E; e += 32) c += ku[e] >= cand ? 1u : 0u;
+      if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)top_k) v = cand;
+    }
+    // 3. candidates
+    const uint32_t thr = f32_to_key(key_to_f32(v) - 2.0f * kKeyTol);
+    int nc = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const bool c = e < E && ku[e] >= thr;
+      const unsigned m = __ballot_sync(0xffffffffu, c);
+      if (c) cid[nc + __popc(m & ((1u << lane) - 1u))] = e;
+      nc += __popc(m);
     }
     __syncwarp();
-    for (int k = 0; k < top_k; ++k) {
-      bool v = bv; double kk = bk; int ee = be;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        bool v2 = __shfl_down_sync(0xffffffffu, v, o);
-        double k2 = __shfl_down_sync(0xffffffffu, kk, o);
-        int e2 = __shfl_down_sync(0xffffffffu, ee, o);
-        if (lane + o < 32 && topk_better(v2, k2, e2, v, kk, ee)) { v = v2; kk = k2; ee = e2; }
-      }
-      ee = __shfl_sync(0xffffffffu, ee, 0);
-      if (lane == 0) idx_out[(size_t)t * top_k + k] = ee;
-      if ((ee & 31) == lane) {
-        taken[ee] = 1;
-        bv = false;
-        for (int e = lane; e < n_experts; e += 32) {
-          if (taken[e]) continue;
-          double kv = keys[e];
-          if (!bv || kv > bk) { bv = true; bk = kv; be = e; }
+    for (int j = lane; j < nc; j += 32) {
+      const int e = cid[j];
+      ckey[j] = sigmoid_f64((double)lrow[e]) - s_alpha[e];
+    }
+    __syncwarp();
+    // 4. exact selection among the candidates
+    if (nc <= 32) {
+      if (lane < nc) {
+        const double kj = ckey[lane];
+        const int ej = cid[lane];
+        int rank = 0;
+        for (int i = 0; i < nc; ++i) {
+          const double ki = ckey[i];
+          rank += (ki > kj || (ki == kj && cid[i] < ej)) ? 1 : 0;
+        }
+        if (rank < top_k) {
+          idx_out[(size_t)t * top_k + rank] = ej;
+          chosen_s[rank] = (double)ej;
         }
       }
-      if (lane == 0) chosen_s[k] = (double)ee;  // expert id, converted back below
-      __syncwarp();
+    } else {
+      bool bv = false;
+      double bk = 0.0;
+      int be = 0;
+      for (int j = lane; j < nc; j += 32)
+        if (topk_better(true, ckey[j], cid[j], bv, bk, be)) { bv = true; bk = ckey[j]; be = cid[j]; }
+      for (int k = 0; k < top_k; ++k) {
+        bool wv = bv;
+        double wk = bk;
+        int we = be;
+        warp_best(wv, wk, we);
+        if (lane == 0) {
+          idx_out[(size_t)t * top_k + k] = we;
+          chosen_s[k] = (double)we;
+        }
+        if (bv && be == we) {
+          // this lane held the winner (each expert is one candidate): drop it and rescan
+          bv = false;
+          for (int j = lane; j < nc; j += 32) {
+            if (cid[j] == we) ckey[j] = kTaken64;
+            const double kd = ckey[j];
+            if (kd == kTaken64) continue;
+            if (topk_better(true, kd, cid[j], bv, bk, be)) { bv = true; bk = kd; be = cid[j]; }
+          }
+        }
+      }
     }
+    __syncwarp();
     // combine weights: chosen raw scores over their sum (summed in k order, fp64)
     for (int k = lane; k < top_k; k += 32) {
-      int e = (int)chosen_s[k];
+      const int e = (int)chosen_s[k];
       chosen_s[k] = sigmoid_f64((double)lrow[e]);
     }
     __syncwarp();
@@ -174,9 +248,17 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
   }
 }
 
-size_t topk_smem_bytes(int n_experts) {
-  return (size_t)(kTopkWarps + 1) * n_experts * sizeof(double) + kTopkWarps * 64 * sizeof(double) +
-         (size_t)kTopkWarps * n_experts;
+size_t topk_smem_bytes(int n_experts, int nwarps) {
+  return (size_t)(nwarps + 1) * n_experts * sizeof(double) + (size_t)nwarps * kMaxTopK * sizeof(double) +
+         (size_t)n_experts * sizeof(float) + (size_t)nwarps * 2 * n_experts * sizeof(uint32_t);
+}
+
+// Warps per block that fit the shared-memory budget (at least one; a single warp may
+// exceed the budget slightly at the largest expert count, which the launch attribute allows).
+int topk_warps(int n_experts) {
+  int w = kTopkMaxWarps;
+  while (w > 1 && topk_smem_bytes(n_experts, w) > kTopkSmemCap) --w;
+  return w;
 }
 
 // ------------------------------------------------------------------------------------
@@ -340,11 +422,12 @@ cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st) {
   if (a.bt <= 0) return cudaSuccess;
   qb_cutoff_kernel<<<a.n_experts, kCutoffThreads, 0, st>>>(a.logits_t, a.bt, a.n_experts, a.top_k,
                                                           a.alpha);
-  const size_t tk_smem = topk_smem_bytes(a.n_experts);
-  int tk_grid = (a.bt + kTopkWarps - 1) / kTopkWarps;
+  const int tk_warps = topk_warps(a.n_experts);
+  const size_t tk_smem = topk_smem_bytes(a.n_experts, tk_warps);
+  int tk_grid = (a.bt + tk_warps - 1) / tk_warps;
   if (tk_grid > 148 * 16) tk_grid = 148 * 16;
-  topk_kernel<<<tk_grid, kTopkWarps * 32, tk_smem, st>>>(a.logits, a.alpha, a.bt, a.n_experts,
-                                                        a.top_k, a.idx, a.w);
+  topk_kernel<<<tk_grid, tk_warps * 32, tk_smem, st>>>(a.logits, a.alpha, a.bt, a.n_experts,
+                                                      a.top_k, a.idx, a.w);
   const int nblk = (a.bt + kSegTokens - 1) / kSegTokens;
   const size_t seg_smem = (size_t)kSegWarps * a.n_experts * sizeof(uint32_t);
   seg_count_kernel<<<nblk, kSegThreads, seg_smem, st>>>(a.idx, a.bt, a.top_k, a.n_experts,
@@ -372,7 +455,7 @@ cudaError_t launch_segments(const int32_t* idx, int bt, int top_k, int n_experts
 cudaError_t route_tail_prepare() {
   // dynamic shared memory above 48 KB for the largest supported expert count
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)topk_smem_bytes(kMaxExperts));
+                                       (int)topk_smem_bytes(kMaxExperts, topk_warps(kMaxExperts)));
   if (e != cudaSuccess) return e;
   const int seg = kSegWarps * kMaxExperts * (int)sizeof(uint32_t);
   e = cudaFuncSetAttribute(seg_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, seg);
