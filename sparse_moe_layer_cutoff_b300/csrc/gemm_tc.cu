@@ -573,12 +573,20 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             float* o = static_cast<float*>(p.out) + row0 * p.ldo + fout;
             float* ot = p.out_t + (long long)fout * p.ldt + row0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nj) {
-                const float val = __uint_as_float(v[j]) + bias;
-                o[(long long)j * p.ldo] = val;
-                ot[j] = val;
-              }
+            for (int j = 0; j < 32; ++j) {
+              v[j] = __float_as_uint(__uint_as_float(v[j]) + bias);
+              if (j < nj) o[(long long)j * p.ldo] = __uint_as_float(v[j]);
+            }
+            // the transposed row: this lane's 32 consecutive tokens, 16-byte stores when aligned
+            if (nj == 32 && (reinterpret_cast<uintptr_t>(ot) & 15u) == 0) {
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<uint4*>(ot + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nj) ot[j] = __uint_as_float(v[j]);
+            }
           }
         }
       }
@@ -663,6 +671,22 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token tile of a dense GEMM: the multiple of 16 in [128, kTokMax] that minimises
+// waves x (tile + a fixed per-tile cost of 32 tokens), so the last wave of the persistent
+// grid is nearly full (e.g. the 8192-token router: 172 tiles of 192 tokens leave most of
+// the second wave idle; 256 tiles of 128 fill it, and narrow tiles double-buffer TMEM).
+int dense_tok_tile(int bt, int n_fb, int grid) {
+  int best = kTokMax;
+  long long best_cost = -1;
+  for (int tt = kTokMax; tt >= 128; tt -= 16) {
+    const long long tiles = (long long)((bt + tt - 1) / tt) * n_fb;
+    const long long waves = (tiles + grid - 1) / grid;
+    const long long cost = waves * (tt + 32);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = tt; }
+  }
+  return best;
 }
 
 }  // namespace
@@ -798,6 +822,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   }
   if (!ok) return cudaErrorInvalidValue;
   p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
+  if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, pl->sm_count);
   int grid = pl->sm_count;
   if (p.G == 0) {
     const long long tiles = (long long)((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb;
