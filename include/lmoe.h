@@ -166,6 +166,18 @@ typedef struct {
 
 LMOE_API lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* out);
 
+/* Streaming cutoffs: a variant of the per-call cutoff for callers that route a stream of
+ * batches ("KimiK3的StableLatentMoE架构解析", ¶"第三": alpha is adjusted dynamically so each
+ * expert's count approaches its quantile target).  With momentum m in [0, 1), every
+ * lmoe_route / lmoe_forward on this context uses
+ *     alpha = m * alpha_prev + (1 - m) * alpha_batch      (fp64, each step rounded)
+ * where alpha_batch is the call's own quantile cutoff and alpha_prev the cutoff the
+ * previous call on this context used; the first call after this function uses
+ * alpha_batch.  m = 0 (the default) gives per-call cutoffs.  The state lives in the
+ * context's workspace and follows stream order.  Returns LMOE_ERR_INVALID_ARG for a NULL
+ * context or m outside [0, 1); no GPU work. */
+LMOE_API lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum);
+
 /* Per-stage device timing.  lmoe_profile(ctx, 1) clears the record and starts recording
  * CUDA events on the call's stream at every stage boundary of each lmoe_forward (up to
  * 1024 calls); lmoe_profile(ctx, 0) stops.  lmoe_profile_read synchronises on the

@@ -106,6 +106,20 @@ def quantile_cutoff(s: np.ndarray, top_k: int) -> np.ndarray:
     return vj + frac * (v[j + 1] - vj)
 
 
+def streaming_cutoff(alpha_batch: np.ndarray, alpha_prev: np.ndarray | None, momentum: float) -> np.ndarray:
+    """Cutoff carried across calls ([K3-news] ¶"第三": alpha is "dynamically adjusted" so
+    that each expert's count approaches its quantile target).  Reading taken for this
+    variant of A5: an exponential moving average of the per-call quantile,
+        alpha = m * alpha_prev + (1 - m) * alpha_batch,
+    evaluated in that order in fp64 with no fused multiply-add; with no previous cutoff
+    (the first call) or m = 0 it is alpha_batch itself (A5)."""
+    alpha_batch = np.asarray(alpha_batch, np.float64)
+    if alpha_prev is None or momentum == 0.0:
+        return alpha_batch.copy()
+    m = np.float64(momentum)
+    return m * np.asarray(alpha_prev, np.float64) + (np.float64(1.0) - m) * alpha_batch
+
+
 def topk_select(s: np.ndarray, alpha: np.ndarray, top_k: int) -> tuple[np.ndarray, np.ndarray]:
     """Per token, the K experts with the largest key s - alpha (A6), ties to the lower
     expert index, listed by key descending (A7) ([K3-news] ¶"具体前向流程": top-16).
@@ -155,9 +169,10 @@ def permutation(idx: np.ndarray, n_experts: int):
     return offsets.astype(np.int32), perm, inv.reshape(bt, top_k).astype(np.int32)
 
 
-def route(logits: np.ndarray, top_k: int) -> dict:
+def route(logits: np.ndarray, top_k: int, alpha_prev: np.ndarray | None = None, momentum: float = 0.0) -> dict:
     """The whole router on given logits (which already hold any bias): sigmoid scores,
-    per-expert cutoffs, top-K, combine weights, counts and segments.
+    per-expert cutoffs, top-K, combine weights, counts and segments.  With momentum > 0
+    and the previous call's cutoff, the cutoff is the streaming one (streaming_cutoff).
 
     Also reports `min_gap`: the smallest non-zero difference between adjacent keys among
     each token's K+1 largest.  A selection computed elsewhere from the same logits in
@@ -165,7 +180,7 @@ def route(logits: np.ndarray, top_k: int) -> dict:
     l = np.asarray(logits, np.float64)
     bt, n_experts = l.shape
     s = sigmoid(l)
-    alpha = quantile_cutoff(s, top_k)
+    alpha = streaming_cutoff(quantile_cutoff(s, top_k), alpha_prev, momentum)
     idx, sorted_keys = topk_select(s, alpha, top_k)
     w = combine_weights(s, idx)
     counts = expert_counts(idx, n_experts)

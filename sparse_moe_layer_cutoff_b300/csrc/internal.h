@@ -17,6 +17,9 @@ struct RouteArgs {
   const float* logits_t;    // [E, bt]
   int bt, n_experts, top_k, tile_m;
   double* alpha;            // [E]
+  const double* alpha_prev; // [E] previous call's cutoff (streaming cutoffs), or null
+  double momentum;          // weight of alpha_prev
+  double* alpha_state;      // [E] where this call's cutoff is kept for the next, or null
   int32_t* idx;             // [bt, K]
   float* w;                 // [bt, K]
   int32_t* block_cnt;       // [ceil(bt / kSegTokens), E]

@@ -27,12 +27,15 @@ struct lmoe_ctx {
   bool check;
   bool use_tc;
   int last_bt;
+  double momentum;      // streaming cutoffs: weight of the previous call's cutoff (0 = per call)
+  bool state_valid;     // a call has stored its cutoff since momentum was set
   // workspace (one allocation)
   char* ws;
   size_t ws_bytes;
   float* logits;
   float* logits_t;
   double* alpha;
+  double* alpha_state;
   int32_t* idx;
   float* wk;
   int32_t* block_cnt;
@@ -159,8 +162,13 @@ cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, in
   r.block_cnt = ctx->block_cnt; r.counts = ctx->counts; r.offsets = ctx->offsets;
   r.mtile_off = ctx->mtile_off; r.perm = ctx->perm; r.inv = ctx->inv;
   r.user_counts = user_counts;
+  r.momentum = ctx->momentum;
+  r.alpha_prev = (ctx->momentum > 0.0 && ctx->state_valid) ? ctx->alpha_state : nullptr;
+  r.alpha_state = ctx->momentum > 0.0 ? ctx->alpha_state : nullptr;
   ctx->launches += kRouteTailLaunches;
-  return launch_route_tail(r, st);
+  e = launch_route_tail(r, st);
+  if (e == cudaSuccess && ctx->momentum > 0.0) ctx->state_valid = true;
+  return e;
 }
 
 }  // namespace
@@ -229,6 +237,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   size_t o_logits = cv.take<float>(bt * E);
   size_t o_logits_t = cv.take<float>(bt * E);
   size_t o_alpha = cv.take<double>(E);
+  size_t o_alpha_state = cv.take<double>(E);
   size_t o_idx = cv.take<int32_t>(bt * K);
   size_t o_w = cv.take<float>(bt * K);
   size_t o_bcnt = cv.take<int32_t>(nblk * E);
@@ -253,6 +262,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   ctx->logits = (float*)(b + o_logits);
   ctx->logits_t = (float*)(b + o_logits_t);
   ctx->alpha = (double*)(b + o_alpha);
+  ctx->alpha_state = (double*)(b + o_alpha_state);
   ctx->idx = (int32_t*)(b + o_idx);
   ctx->wk = (float*)(b + o_w);
   ctx->block_cnt = (int32_t*)(b + o_bcnt);
@@ -408,6 +418,13 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
   }
   if (ctx->prof_on && ctx->prof_calls < kProfCap) ctx->prof_calls++;
   return finish(ctx, st, e);
+}
+
+lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum) {
+  if (!ctx || !(momentum >= 0.0 && momentum < 1.0)) return LMOE_ERR_INVALID_ARG;
+  ctx->momentum = momentum;
+  ctx->state_valid = false;
+  return LMOE_OK;
 }
 
 lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable) {

@@ -21,7 +21,8 @@ constexpr int kCutoffThreads = 256;
 
 __global__ void __launch_bounds__(kCutoffThreads)
 qb_cutoff_kernel(const float* __restrict__ logits_t, int bt, int n_experts, int top_k,
-                 double* __restrict__ alpha) {
+                 double* __restrict__ alpha, const double* __restrict__ alpha_prev, double momentum,
+                 double* __restrict__ alpha_state) {
   const int e = blockIdx.x;
   const float* col = logits_t + (size_t)e * bt;
   __shared__ uint32_t hist[256];
@@ -96,7 +97,11 @@ qb_cutoff_kernel(const float* __restrict__ logits_t, int bt, int n_experts, int 
       // no fused multiply-add: the same rounding as a plain a + f * (b - a)
       a = __dadd_rn(vj, __dmul_rn(frac, __dsub_rn(vj1, vj)));
     }
+    // streaming variant: a moving average with the previous call's cutoff, evaluated as
+    // m * prev + (1 - m) * a, each step rounded (no fused multiply-add)
+    if (alpha_prev) a = __dadd_rn(__dmul_rn(momentum, alpha_prev[e]), __dmul_rn(__dsub_rn(1.0, momentum), a));
     alpha[e] = a;
+    if (alpha_state) alpha_state[e] = a;
   }
 }
 
@@ -420,8 +425,8 @@ seg_scatter_kernel(const int32_t* __restrict__ idx, int bt, int top_k, int n_exp
 // ------------------------------------------------------------------------------------
 cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st) {
   if (a.bt <= 0) return cudaSuccess;
-  qb_cutoff_kernel<<<a.n_experts, kCutoffThreads, 0, st>>>(a.logits_t, a.bt, a.n_experts, a.top_k,
-                                                          a.alpha);
+  qb_cutoff_kernel<<<a.n_experts, kCutoffThreads, 0, st>>>(a.logits_t, a.bt, a.n_experts, a.top_k, a.alpha,
+                                                          a.alpha_prev, a.momentum, a.alpha_state);
   const int tk_warps = topk_warps(a.n_experts);
   const size_t tk_smem = topk_smem_bytes(a.n_experts, tk_warps);
   int tk_grid = (a.bt + tk_warps - 1) / tk_warps;

@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_status_string.restype = ctypes.c_char_p
     lib.lmoe_workspace.argtypes = [c_vp, ctypes.POINTER(lmoe_workspace_view)]
     lib.lmoe_workspace.restype = c_i32
+    lib.lmoe_set_cutoff_momentum.argtypes = [c_vp, ctypes.c_double]
+    lib.lmoe_set_cutoff_momentum.restype = c_i32
     lib.lmoe_profile.argtypes = [c_vp, c_i32]
     lib.lmoe_profile.restype = c_i32
     lib.lmoe_profile_read.argtypes = [c_vp, ctypes.POINTER(c_f32), ctypes.POINTER(c_i32),
@@ -135,6 +137,11 @@ def lmoe_workspace(ctx) -> lmoe_workspace_view:
 LMOE_NUM_STAGES = 8
 STAGE_NAMES = ("router_gemm", "cutoff_topk_segments", "w_down_gemm", "expert_gate_up_gemm",
                "expert_down_gemm", "rmsnorm_combine", "shared_gate_up_gemm", "up_shared_down_gemm")
+
+
+def lmoe_set_cutoff_momentum(ctx, momentum: float) -> int:
+    """Streaming cutoffs: alpha = m * previous alpha + (1 - m) * this batch's quantile."""
+    return load_library().lmoe_set_cutoff_momentum(c_vp(ctx), float(momentum))
 
 
 def lmoe_profile(ctx, enable: bool) -> int:
@@ -231,6 +238,12 @@ class LatentMoE:
 
     def sync_status(self, stream=None) -> int:
         return lmoe_sync_status(self.ctx, self._stream(stream))
+
+    def set_cutoff_momentum(self, momentum: float) -> None:
+        """Streaming cutoffs across calls (0 = per-call cutoffs); resets the carried state."""
+        st = lmoe_set_cutoff_momentum(self.ctx, momentum)
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_set_cutoff_momentum")
 
     def workspace(self) -> lmoe_workspace_view:
         return lmoe_workspace(self.ctx)

@@ -11,7 +11,8 @@ from oracle import lmoe_oracle as O
 from sparse_moe_layer_cutoff_b300 import LatentMoE, LmoeError
 from sparse_moe_layer_cutoff_b300 import lmoe as L
 from tests.lmoe_testing import Run, oracle_weights, rel_l2, to64
-from workloads import WORKLOADS, LayerShape, Workload, make_inputs
+from sparse_moe_layer_cutoff_b300.lmoe import workspace_tensors
+from workloads import WORKLOADS, LayerShape, Workload, make_inputs, make_x
 
 pytestmark = pytest.mark.gpu
 
@@ -196,3 +197,60 @@ def test_full_skewed_bt16384():
     nrep = r.bt // 4
     assert torch.equal(r.out[:nrep], r.out[:1].expand(nrep, -1))
     r.close()
+
+
+@pytest.mark.parametrize("scale_log2", [-20, -23])
+def test_near_tie_routing_is_exact(scale_log2):
+    """Router keys that differ by ~1e-6 between experts, inside the band where the fp32
+    prefilter cannot order them: the top-K must still match the fp64 selection bit for bit.
+    All router rows are equal except column 0, which gives expert e the slope (e+1)*2^s, so
+    the logits of a token differ across experts only by x[t,0] (e+1) 2^s."""
+    w = WORKLOADS["small_bf16"].with_(seed=21)
+    x, weights, bias = make_inputs(w, "cuda", 333)
+    wr = weights["w_router"][0:1].repeat(w.shape.n_experts, 1)
+    wr[:, 0] = (torch.arange(1, w.shape.n_experts + 1, device="cuda", dtype=torch.float32) *
+                2.0 ** scale_log2).to(wr.dtype)
+    weights = dict(weights, w_router=wr.contiguous())
+    r = Run(w, x=x, weights=weights, bias=bias)
+    assert r.status == 0
+    ref = r.check_routing()
+    r.check_output(ref_route=ref)
+
+
+def test_streaming_cutoff_matches_oracle():
+    """lmoe_set_cutoff_momentum: each call's cutoff is m * previous + (1 - m) * the call's
+    quantile, carried in the context; routing stays bit-exact against the oracle's
+    streaming cutoff given the same logits, and a new momentum restarts the stream."""
+    wl = WORKLOADS["small_bf16"]
+    x0, weights, _ = make_inputs(wl, "cuda", 300)
+    layer = LatentMoE(SMALL, weights, max_bt=300)
+    layer.set_cutoff_momentum(0.75)
+    K = SMALL.top_k
+    prev = None
+    for i in range(3):
+        xb = make_x(wl, "cuda", 300, seed_offset=40 + i)
+        r = layer.route(xb)
+        torch.cuda.synchronize()
+        ref = O.route(to64(r["logits"]), K, alpha_prev=prev, momentum=0.75)
+        assert ref["min_gap"] > 1e-12
+        np.testing.assert_allclose(r["alpha"].cpu().numpy(), ref["alpha"], rtol=1e-15, atol=0)
+        np.testing.assert_array_equal(r["idx"].cpu().numpy(), ref["idx"])
+        np.testing.assert_array_equal(r["counts"].cpu().numpy(), ref["counts"])
+        prev = ref["alpha"]
+    # a forward advances the same stream (its cutoff and selection, read from the workspace)
+    layer.forward(x0)
+    torch.cuda.synchronize()
+    ws = workspace_tensors(layer)
+    ref = O.route(to64(ws["logits"]), K, alpha_prev=prev, momentum=0.75)
+    np.testing.assert_allclose(ws["alpha"].cpu().numpy(), ref["alpha"], rtol=1e-15, atol=0)
+    np.testing.assert_array_equal(ws["idx"].cpu().numpy(), ref["idx"])
+    assert layer.sync_status() == 0
+    # restarting: momentum 0 gives per-call cutoffs again
+    layer.set_cutoff_momentum(0.0)
+    r = layer.route(x0)
+    torch.cuda.synchronize()
+    ref = O.route(to64(r["logits"]), K)
+    np.testing.assert_allclose(r["alpha"].cpu().numpy(), ref["alpha"], rtol=1e-15, atol=0)
+    with pytest.raises(LmoeError):
+        layer.set_cutoff_momentum(1.0)
+    layer.close()

@@ -87,3 +87,16 @@ def test_unstable_segments_are_caught(monkeypatch):
         return off, perm, inv
     monkeypatch.setattr(O, "permutation", bad_perm)
     assert _fails(lambda: P.test_topk_and_segments_brute_force(64, 16, 4))
+
+
+def test_streaming_cutoff_swapped_momentum_is_caught(monkeypatch):
+    # m weighting the batch quantile instead of the previous cutoff
+    monkeypatch.setattr(O, "streaming_cutoff", lambda ab, ap, m:
+                        np.asarray(ab, np.float64).copy() if ap is None or m == 0.0 else
+                        (1.0 - m) * np.asarray(ap) + m * np.asarray(ab))
+    assert _fails(P.test_streaming_cutoff_decays_geometrically)
+
+
+def test_streaming_cutoff_ignoring_state_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "streaming_cutoff", lambda ab, ap, m: np.asarray(ab, np.float64).copy())
+    assert _fails(P.test_streaming_cutoff_decays_geometrically)

@@ -101,6 +101,47 @@ def test_quantile_special_cases():
     np.testing.assert_array_equal(O.quantile_cutoff(c, 1), np.full(3, 0.25))
 
 
+def test_streaming_cutoff_reduces_to_per_call_quantile():
+    """Momentum 0, or no previous cutoff, is the per-call quantile (reading A5) exactly."""
+    rng = np.random.default_rng(5)
+    logits = rng.normal(size=(300, 16))
+    per_call = O.quantile_cutoff(O.sigmoid(logits), 4)
+    prev = rng.uniform(size=16)
+    np.testing.assert_array_equal(O.route(logits, 4, alpha_prev=prev, momentum=0.0)["alpha"], per_call)
+    np.testing.assert_array_equal(O.route(logits, 4, alpha_prev=None, momentum=0.9)["alpha"], per_call)
+
+
+def test_streaming_cutoff_decays_geometrically():
+    """One batch with quantiles q1, then calls that all see q2: the cutoff after call n is
+    q2 + m^(n-1) (q1 - q2) (closed form of the moving average), and it stays between the
+    previous cutoff and the batch quantile at every call."""
+    rng = np.random.default_rng(6)
+    l1 = rng.normal(size=(200, 12))
+    l2 = rng.normal(loc=0.5, size=(200, 12))
+    m, K = 0.8, 3
+    q1 = O.quantile_cutoff(O.sigmoid(l1), K)
+    q2 = O.quantile_cutoff(O.sigmoid(l2), K)
+    a = O.route(l1, K, alpha_prev=None, momentum=m)["alpha"]
+    np.testing.assert_array_equal(a, q1)
+    for n in range(2, 8):
+        nxt = O.route(l2, K, alpha_prev=a, momentum=m)["alpha"]
+        lo, hi = np.minimum(a, q2), np.maximum(a, q2)
+        assert np.all(nxt >= lo - 1e-15) and np.all(nxt <= hi + 1e-15)
+        np.testing.assert_allclose(nxt, q2 + math.pow(m, n - 1) * (q1 - q2), rtol=0, atol=1e-14)
+        a = nxt
+
+
+def test_streaming_cutoff_fixed_point():
+    """A stream of identical batches keeps the cutoff at their quantile."""
+    rng = np.random.default_rng(7)
+    logits = rng.normal(size=(150, 10))
+    q = O.quantile_cutoff(O.sigmoid(logits), 2)
+    a = None
+    for _ in range(5):
+        a = O.route(logits, 2, alpha_prev=a, momentum=0.6)["alpha"]
+        np.testing.assert_allclose(a, q, rtol=1e-15, atol=0)
+
+
 # ----------------------------------------------------------------- top-K, weights, segments
 
 def _brute_topk(keys, K):
