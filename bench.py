@@ -29,7 +29,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-from workloads import WORKLOADS, make_inputs, make_x  # noqa: E402
+from workloads import FFN_WORKLOADS, WORKLOADS, make_ffn_inputs, make_inputs, make_x  # noqa: E402
 
 DEFAULT_WORKLOAD = "full_prefill_bt8192"
 METRIC = "LatentMoE layer fwd tokens/s on 1 B300; % of bf16 TC peak (or HBM BW)"
@@ -252,13 +252,103 @@ def run_reference(args, ws, rank):
     return 0
 
 
+def run_ffn(args, ws, rank, local):
+    """The dense first-layer SiTU-GLU FFN (out = W_down act(W_gate x, W_up x)) through
+    lmoe_ffn_forward: same timing rules as the layer; the reference arm times the oracle."""
+    from oracle import lmoe_oracle as O
+
+    w = FFN_WORKLOADS[args.workload]
+    flops = 2 * w.bt * 3 * w.d * w.inter
+    metric = "dense SiTU-GLU FFN fwd tokens/s on 1 B300"
+    cfg = {"workload": w.name, "bt": w.bt, "d": w.d, "inter": w.inter, "global_batch": w.bt * ws,
+           "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"}
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        x, wg, wu, wd = make_ffn_inputs(w, "cuda" if torch.cuda.is_available() else "cpu", 8)
+        W = [t.cpu().to(torch.float64).numpy() for t in (wg, wu, wd)]
+        xs = x.cpu().to(torch.float64).numpy()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            O.dense_ffn(xs[:2], *W, w.beta, w.beta_u)
+        dt = time.perf_counter() - t0
+        value = 2 * args.steps / dt
+        print(json.dumps({"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": 1,
+                          "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                          "data": "synthetic", "config": cfg,
+                          "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _blas_threads(),
+                                           "kind": "oracle", "sample": "2 tokens per step"},
+                          "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    from sparse_moe_layer_cutoff_b300 import DenseFFN
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    x, wg, wu, wd = make_ffn_inputs(w, device)
+    ffn = DenseFFN(w.d, w.inter, wg, wu, wd, max_bt=w.bt, beta=w.beta, beta_u=w.beta_u)
+    out = torch.empty((w.bt, w.d), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(args.warmup):
+        ffn.forward(x, out)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        ffn.forward(x, out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier(ws)
+    if ffn.sync_status() != 0:
+        raise RuntimeError("device status set in the timed region")
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, device)
+    value = sum_over_ranks(float(w.bt * args.steps), ws, device) / (ms / 1e3)
+    step_s = ms / 1e3 / args.steps
+    pk = peaks()
+    tc_peak = pk["tc_sustained"] if ms / 1e3 > 2.0 else pk["tc"]
+    achieved = flops / step_s / 1e12
+    roof = {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s", "frac": achieved / tc_peak,
+            "traffic": None, "kernel": "dense_ffn (SiTU-GLU + down)", "ms_per_launch": step_s * 1e3,
+            "algorithmic_flops": flops,
+            "peak_source": pk["source"] + (" sustained" if ms / 1e3 > 2.0 else " burst")}
+    xh = x.cpu().pin_memory()
+    oh = torch.empty((w.bt, w.d), dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty_like(x)
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        ffn.forward(xd, out)
+        oh.copy_(out, non_blocking=True)
+    e3.record(stream)
+    torch.cuda.synchronize()
+    e2e = w.bt * args.e2e_steps / (e2.elapsed_time(e3) / 1e3)
+    if rank == 0:
+        print(json.dumps({"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+                          "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+                          "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                          "config": cfg, "roofline": roof, "cpu_baseline": None,
+                          "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": w.bt * w.d * 2,
+                                  "d2h_bytes_per_step": w.bt * w.d * 2},
+                          "gpu_launches": 2 * args.steps, "clocks": clk}), flush=True)
+    ffn.close()
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="lmoe", choices=["lmoe", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS) + sorted(FFN_WORKLOADS))
     ap.add_argument("--cpu-tokens", type=int, default=12, help="oracle sample for cpu_baseline")
     ap.add_argument("--cpu-tokens-ref", type=int, default=2, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -267,6 +357,8 @@ def main(argv=None):
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup()
+    if args.workload in FFN_WORKLOADS:
+        return run_ffn(args, ws, rank, local)
     if args.impl == "reference":
         rc = run_reference(args, ws, rank)
         barrier(ws)

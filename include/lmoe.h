@@ -212,6 +212,39 @@ LMOE_API lmoe_status lmoe_segments_noalloc(const int32_t* topk_idx, int32_t bt, 
                                            int32_t n_experts, int32_t* expert_counts, int32_t* offsets,
                                            int32_t* perm, int32_t* inv, lmoe_stream stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Dense SiTU-GLU FFN: the full-width feed-forward block of the model's first (dense) layer
+ * ("Vue d'ensemble de l'architecture", mkdocs.reaper.mx, table "Le budget de paramètres,
+ * module par module": 727 M parameters, intermediate 33 792 at d = 7168), with the experts'
+ * activation ("KimiK3的StableLatentMoE架构解析", ¶"第一"):
+ *   out[t] = W_down act(W_gate x[t], W_up x[t]),  act as for the layer above.
+ * bf16 only, on the tensor-core engine; d and inter multiples of 64.
+ * --------------------------------------------------------------------------------------- */
+typedef struct {
+  int32_t d;        /* model width                          (7168)  */
+  int32_t inter;    /* intermediate width                   (33792) */
+  float beta;       /* SiTU-GLU gate bound                  (4)     */
+  float beta_u;     /* SiTU-GLU up bound                    (25)    */
+} lmoe_ffn_config;
+
+typedef struct lmoe_ffn lmoe_ffn;
+
+/* Borrows w_gate [inter, d], w_up [inter, d], w_down [d, inter] (bf16, device, 16-byte
+ * aligned; they must outlive the context) and allocates an activation buffer of
+ * max_bt * inter bf16.  Errors as for lmoe_create (INVALID_ARG: bad sizes or pointers;
+ * UNSUPPORTED: d or inter not a multiple of 64; OOM; CUDA). */
+LMOE_API lmoe_status lmoe_ffn_create(const lmoe_ffn_config* cfg, const void* w_gate, const void* w_up,
+                                     const void* w_down, int32_t max_bt, lmoe_ffn** out);
+/* out [bt, d] bf16 = the FFN of x [bt, d] bf16, on `stream` (asynchronous; two kernels).
+ * bt == 0 does nothing; bt > max_bt, NULL or misaligned pointers, or out overlapping x
+ * give LMOE_ERR_INVALID_ARG.  A context is used by one stream at a time. */
+LMOE_API lmoe_status lmoe_ffn_forward(lmoe_ffn* ffn, const void* x, int32_t bt, void* out, lmoe_stream stream);
+/* Synchronises `stream` and returns (then clears) the device status of this context's
+ * kernels (LMOE_ERR_TIMEOUT when a bounded device-side wait ran out). */
+LMOE_API lmoe_status lmoe_ffn_sync_status(lmoe_ffn* ffn, lmoe_stream stream);
+/* NULL-safe; synchronises the device, frees the activation buffer. */
+LMOE_API void lmoe_ffn_destroy(lmoe_ffn* ffn);
+
 /* Library build identifier (static string): engine names per dtype. */
 LMOE_API const char* lmoe_build_info(void);
 

@@ -255,6 +255,14 @@ def shared_experts(x: np.ndarray, weights, beta: float, beta_u: float) -> np.nda
     return out
 
 
+def dense_ffn(x: np.ndarray, w_gate, w_up, w_down, beta: float = 4.0, beta_u: float = 25.0) -> np.ndarray:
+    """The dense first layer's feed-forward block: W_down act(W_gate x, W_up x) with the
+    experts' SiTU-GLU ([K3-arch] "Le budget de paramètres, module par module": one dense FFN
+    of 727 M parameters, intermediate 33 792 at d = 7168; the activation is reading A1)."""
+    x = _f64(x)
+    return situ_glu(x @ _f64(w_gate).T, x @ _f64(w_up).T, beta, beta_u) @ _f64(w_down).T
+
+
 def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float = 4.0,
                   beta_u: float = 25.0, eps: float = 1e-6, return_parts: bool = False):
     """Stable LatentMoE layer output for the rows of x, given their routing (idx, w).

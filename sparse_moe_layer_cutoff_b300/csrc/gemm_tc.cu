@@ -689,6 +689,23 @@ int dense_tok_tile(int bt, int n_fb, int grid) {
   return best;
 }
 
+// One launch of the persistent kernel: grid = SMs (fewer when a dense GEMM has fewer tiles).
+cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st) {
+  if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, sm_count);
+  int grid = sm_count;
+  if (p.G == 0) {
+    const long long tiles = (long long)((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb;
+    if (tiles < grid) grid = (int)tiles;
+  }
+  if (grid <= 0) return cudaSuccess;
+  switch (epi) {
+    case kEpiStore: tc_gemm_kernel<kEpiStore><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+    case kEpiGlu: tc_gemm_kernel<kEpiGlu><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+    default: tc_gemm_kernel<kEpiRouter><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 struct TcPlan {
@@ -822,19 +839,87 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   }
   if (!ok) return cudaErrorInvalidValue;
   p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
-  if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, pl->sm_count);
-  int grid = pl->sm_count;
-  if (p.G == 0) {
-    const long long tiles = (long long)((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb;
-    if (tiles < grid) grid = (int)tiles;
+  return launch_tc(maps, p, epi, pl->sm_count, st);
+}
+
+// ------------------------------------------------------------------ dense SiTU-GLU FFN
+struct TcFfnPlan {
+  int d, inter, sm_count;
+  float beta, beta_u;
+  void* h;
+  uint32_t* status;
+  CUtensorMap m_gate, m_up, m_down, m_h;
+};
+
+lmoe_status tc_ffn_create(int d, int inter, float beta, float beta_u, const void* w_gate, const void* w_up,
+                          const void* w_down, int max_bt, int sm_count, void* h, uint32_t* status, TcFfnPlan** plan) {
+  *plan = nullptr;
+  TcFfnPlan* pl = new (std::nothrow) TcFfnPlan();
+  if (!pl) return LMOE_ERR_OOM;
+  pl->d = d;
+  pl->inter = inter;
+  pl->sm_count = sm_count;
+  pl->beta = beta;
+  pl->beta_u = beta_u;
+  pl->h = h;
+  pl->status = status;
+  const bool ok = make_map(&pl->m_gate, w_gate, inter, d, d, kHalf) && make_map(&pl->m_up, w_up, inter, d, d, kHalf) &&
+                  make_map(&pl->m_down, w_down, d, inter, inter, kHalf) &&
+                  make_map(&pl->m_h, h, max_bt, inter, inter, kTokBox);
+  cudaError_t e = ok ? cudaFuncSetAttribute(tc_gemm_kernel<kEpiStore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kSmemBytes)
+                     : cudaErrorInvalidValue;
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete pl;
+    return LMOE_ERR_CUDA;
   }
-  if (grid <= 0) return cudaSuccess;
-  switch (epi) {
-    case kEpiStore: tc_gemm_kernel<kEpiStore><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
-    case kEpiGlu: tc_gemm_kernel<kEpiGlu><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
-    default: tc_gemm_kernel<kEpiRouter><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+  *plan = pl;
+  return LMOE_OK;
+}
+
+void tc_ffn_destroy(TcFfnPlan* plan) { delete plan; }
+
+// h = act(x W_gate^T, x W_up^T), then out = h W_down^T: two launches of the GEMM kernel.
+cudaError_t tc_ffn_forward(TcFfnPlan* pl, const void* x, int bt, void* out, cudaStream_t st) {
+  TcMaps maps;
+  TcParams p;
+  for (int pass = 0; pass < 2; ++pass) {
+    memset(&maps, 0, sizeof(maps));
+    memset(&p, 0, sizeof(p));
+    p.nseg = 1;
+    p.bt = bt;
+    p.beta = pl->beta;
+    p.beta_u = pl->beta_u;
+    p.inv_beta = 1.0f / pl->beta;
+    p.inv_beta_u = 1.0f / pl->beta_u;
+    p.status = pl->status;
+    if (pass == 0) {
+      maps.w[0] = pl->m_gate;
+      maps.wup = pl->m_up;
+      if (!make_map(&maps.tok, x, bt, pl->d, pl->d, kTokBox)) return cudaErrorInvalidValue;
+      p.seg_k0[1] = pl->d;
+      p.n_feat = pl->inter;
+      p.n_fb = (pl->inter + kHalf - 1) / kHalf;
+      p.kblocks = pl->d / kBK;
+      p.out = pl->h;
+      p.ldo = pl->inter;
+    } else {
+      maps.w[0] = pl->m_down;
+      maps.tok = pl->m_h;
+      p.seg_k0[1] = pl->inter;
+      p.n_feat = pl->d;
+      p.n_fb = (pl->d + 2 * kHalf - 1) / (2 * kHalf);
+      p.kblocks = pl->inter / kBK;
+      p.out = out;
+      p.ldo = pl->d;
+    }
+    const cudaError_t e = launch_tc(maps, p, pass == 0 ? kEpiGlu : kEpiStore, pl->sm_count, st);
+    if (e != cudaSuccess) return e;
   }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace lmoe

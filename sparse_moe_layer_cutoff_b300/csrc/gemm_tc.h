@@ -25,4 +25,13 @@ void tc_plan_destroy(TcPlan* plan);
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
 int tc_launches(int op);   // kernels launch_gemm_tc starts for one GemmOp
 
+// Dense SiTU-GLU FFN (out = W_down act(W_gate x, W_up x)) on the same engine: descriptors of
+// the borrowed weights and of the caller-provided h [max_bt, inter] buffer.
+struct TcFfnPlan;
+lmoe_status tc_ffn_create(int d, int inter, float beta, float beta_u, const void* w_gate, const void* w_up,
+                          const void* w_down, int max_bt, int sm_count, void* h, uint32_t* status, TcFfnPlan** plan);
+void tc_ffn_destroy(TcFfnPlan* plan);
+cudaError_t tc_ffn_forward(TcFfnPlan* plan, const void* x, int bt, void* out, cudaStream_t st);
+constexpr int kFfnLaunches = 2;
+
 }  // namespace lmoe

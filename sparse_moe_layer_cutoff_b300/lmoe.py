@@ -35,6 +35,10 @@ class lmoe_weights(ctypes.Structure):
                                     "exp_gate", "exp_up", "exp_down", "sh_gate", "sh_up", "sh_down")]
 
 
+class lmoe_ffn_config(ctypes.Structure):
+    _fields_ = [("d", c_i32), ("inter", c_i32), ("beta", c_f32), ("beta_u", c_f32)]
+
+
 class lmoe_workspace_view(ctypes.Structure):
     _fields_ = [("bt", c_i32)] + [(n, c_vp) for n in ("logits", "alpha", "topk_idx", "topk_w", "offsets",
                                                        "perm", "inv", "z", "h", "y", "cat")]
@@ -72,6 +76,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_status_string.restype = ctypes.c_char_p
     lib.lmoe_workspace.argtypes = [c_vp, ctypes.POINTER(lmoe_workspace_view)]
     lib.lmoe_workspace.restype = c_i32
+    lib.lmoe_ffn_create.argtypes = [ctypes.POINTER(lmoe_ffn_config), c_vp, c_vp, c_vp, c_i32, ctypes.POINTER(c_vp)]
+    lib.lmoe_ffn_create.restype = c_i32
+    lib.lmoe_ffn_forward.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
+    lib.lmoe_ffn_forward.restype = c_i32
+    lib.lmoe_ffn_sync_status.argtypes = [c_vp, c_vp]
+    lib.lmoe_ffn_sync_status.restype = c_i32
+    lib.lmoe_ffn_destroy.argtypes = [c_vp]
+    lib.lmoe_ffn_destroy.restype = None
     lib.lmoe_set_cutoff_momentum.argtypes = [c_vp, ctypes.c_double]
     lib.lmoe_set_cutoff_momentum.restype = c_i32
     lib.lmoe_profile.argtypes = [c_vp, c_i32]
@@ -137,6 +149,25 @@ def lmoe_workspace(ctx) -> lmoe_workspace_view:
 LMOE_NUM_STAGES = 8
 STAGE_NAMES = ("router_gemm", "cutoff_topk_segments", "w_down_gemm", "expert_gate_up_gemm",
                "expert_down_gemm", "rmsnorm_combine", "shared_gate_up_gemm", "up_shared_down_gemm")
+
+
+def lmoe_ffn_create(cfg: lmoe_ffn_config, w_gate: int, w_up: int, w_down: int, max_bt: int):
+    ffn = c_vp()
+    st = load_library().lmoe_ffn_create(ctypes.byref(cfg), c_vp(w_gate), c_vp(w_up), c_vp(w_down), max_bt,
+                                        ctypes.byref(ffn))
+    return st, ffn.value
+
+
+def lmoe_ffn_forward(ffn, x: int, bt: int, out: int, stream: int = 0) -> int:
+    return load_library().lmoe_ffn_forward(c_vp(ffn), c_vp(x), bt, c_vp(out), c_vp(stream))
+
+
+def lmoe_ffn_sync_status(ffn, stream: int = 0) -> int:
+    return load_library().lmoe_ffn_sync_status(c_vp(ffn), c_vp(stream))
+
+
+def lmoe_ffn_destroy(ffn) -> None:
+    load_library().lmoe_ffn_destroy(c_vp(ffn))
 
 
 def lmoe_set_cutoff_momentum(ctx, momentum: float) -> int:
@@ -295,3 +326,49 @@ def workspace_tensors(layer: "LatentMoE") -> dict:
         y=view(v.y, (bt * s.top_k, s.latent), el, fdt),
         cat=view(v.cat, (bt, ldc), el, fdt),
     )
+
+
+class DenseFFN:
+    """Dense SiTU-GLU FFN context over borrowed bf16 torch CUDA weights
+    (w_gate [inter, d], w_up [inter, d], w_down [d, inter])."""
+
+    def __init__(self, d: int, inter: int, w_gate, w_up, w_down, max_bt: int, beta: float = 4.0,
+                 beta_u: float = 25.0):
+        self._keep = (w_gate, w_up, w_down)
+        for t in self._keep:
+            if not t.is_contiguous():
+                raise ValueError("FFN weights must be contiguous")
+        self.d, self.inter, self.max_bt = d, inter, max_bt
+        st, ffn = lmoe_ffn_create(lmoe_ffn_config(d, inter, beta, beta_u), w_gate.data_ptr(), w_up.data_ptr(),
+                                  w_down.data_ptr(), max_bt)
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_ffn_create")
+        self.ffn = ffn
+
+    def forward(self, x, out=None, stream=None):
+        import torch
+
+        if out is None:
+            out = torch.empty((x.shape[0], self.d), dtype=torch.bfloat16, device=x.device)
+        s = torch.cuda.current_stream() if stream is None else stream
+        st = lmoe_ffn_forward(self.ffn, x.data_ptr(), x.shape[0], out.data_ptr(), s.cuda_stream)
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_ffn_forward")
+        return out
+
+    def sync_status(self, stream=None) -> int:
+        import torch
+
+        s = torch.cuda.current_stream() if stream is None else stream
+        return lmoe_ffn_sync_status(self.ffn, s.cuda_stream)
+
+    def close(self):
+        if getattr(self, "ffn", None):
+            lmoe_ffn_destroy(self.ffn)
+            self.ffn = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -100,3 +100,9 @@ def test_streaming_cutoff_swapped_momentum_is_caught(monkeypatch):
 def test_streaming_cutoff_ignoring_state_is_caught(monkeypatch):
     monkeypatch.setattr(O, "streaming_cutoff", lambda ab, ap, m: np.asarray(ab, np.float64).copy())
     assert _fails(P.test_streaming_cutoff_decays_geometrically)
+
+
+def test_dense_ffn_swapped_gate_and_up_is_caught(monkeypatch):
+    orig = O.dense_ffn
+    monkeypatch.setattr(O, "dense_ffn", lambda x, wg, wu, wd, beta=4.0, beta_u=25.0: orig(x, wu, wg, wd, beta, beta_u))
+    assert _fails(P.test_dense_ffn_matches_torch_library_formulation)

@@ -417,3 +417,31 @@ def test_zipf_and_repeated_block_recipe():
     assert torch.equal(x[:10], x[:1].expand(10, -1)) and not torch.equal(x[10], x[0])
     ranks = torch.sort(bias, descending=True).values
     np.testing.assert_allclose(ranks.numpy(), 3.0 * np.arange(1, 17, dtype=np.float64) ** -1.1, rtol=1e-6)
+
+
+# ----------------------------------------------------------------- dense first-layer FFN
+
+def test_dense_ffn_matches_torch_library_formulation():
+    """The oracle's dense FFN against the same expression built from torch library
+    routines in float64 (linear, tanh, sigmoid), on the dense_ffn_small recipe."""
+    from workloads import FFN_WORKLOADS, make_ffn_inputs
+    w = FFN_WORKLOADS["dense_ffn_small"]
+    x, wg, wu, wd = make_ffn_inputs(w, "cpu", 37)
+    x, wg, wu, wd = (t.to(torch.float64) for t in (x, wg, wu, wd))
+    g = F.linear(x, wg) / w.beta
+    u = F.linear(x, wu) / w.beta_u
+    gp = w.beta * torch.tanh(g)
+    want = F.linear(gp * torch.sigmoid(gp) * w.beta_u * torch.tanh(u), wd)
+    got = O.dense_ffn(_np(x), _np(wg), _np(wu), _np(wd), w.beta, w.beta_u)
+    np.testing.assert_allclose(got, want.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_dense_ffn_splits_over_the_intermediate_dimension():
+    """The FFN is a sum over intermediate units: running it on two halves of the units
+    (rows of W_gate / W_up, columns of W_down) and adding equals the whole."""
+    from workloads import FFN_WORKLOADS, make_ffn_inputs
+    x, wg, wu, wd = (_np(t) for t in make_ffn_inputs(FFN_WORKLOADS["dense_ffn_small"], "cpu", 9))
+    h = wg.shape[0] // 2
+    whole = O.dense_ffn(x, wg, wu, wd)
+    parts = O.dense_ffn(x, wg[:h], wu[:h], wd[:, :h]) + O.dense_ffn(x, wg[h:], wu[h:], wd[:, h:])
+    np.testing.assert_allclose(parts, whole, rtol=1e-12, atol=1e-12)

@@ -167,3 +167,43 @@ def make_x(w: Workload, device="cpu", bt: int | None = None, seed_offset: int = 
     if w.repeat_frac > 0 and bt > 0:
         x[: int(round(bt * w.repeat_frac))] = x[0]
     return x
+
+
+# --------------------------------------------------------------------------- dense FFN
+
+@dataclass(frozen=True)
+class FfnWorkload:
+    """The dense first layer's SiTU-GLU FFN ("Vue d'ensemble de l'architecture": 727 M
+    parameters = 3 * 7168 * 33 792)."""
+    name: str
+    d: int
+    inter: int
+    bt: int
+    seed: int
+    beta: float = 4.0
+    beta_u: float = 25.0
+
+
+FFN_WORKLOADS = {
+    w.name: w for w in (
+        FfnWorkload("dense_ffn_small", 1024, 2048, 333, 31),
+        FfnWorkload("dense_ffn_bt8192", 7168, 33792, 8192, 32),
+    )
+}
+
+
+def make_ffn_inputs(w: FfnWorkload, device="cpu", bt: int | None = None):
+    """x [bt, d] ~ N(0, 1), then W_gate, W_up [inter, d] and W_down [d, inter] with std
+    1/sqrt(fan_in), drawn in that order from one seeded generator, rounded once to bf16."""
+    bt = w.bt if bt is None else bt
+    gen = torch.Generator(device=device)
+    gen.manual_seed(w.seed)
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=gen, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+    x = draw((bt, w.d), 1.0)
+    wg = draw((w.inter, w.d), w.d ** -0.5)
+    wu = draw((w.inter, w.d), w.d ** -0.5)
+    wd = draw((w.d, w.inter), w.inter ** -0.5)
+    return x, wg, wu, wd
