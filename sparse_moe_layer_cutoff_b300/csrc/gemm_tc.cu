@@ -628,16 +628,18 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kSlotCols));
 }
 
-// Routed-expert token rows in slot order: zp[slot] = z[perm[slot]] (16-byte vectors).
+// Routed-expert token rows in slot order: zp[slot] = z[perm[slot]]; one warp per row,
+// 16-byte vectors (HBM-bound: each row is read from L2-resident z and written once).
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ z, const int32_t* __restrict__ perm,
                                                           const int32_t* __restrict__ offsets, int n_experts,
                                                           int vec_per_row, uint4* __restrict__ zp) {
-  const long long nslots = offsets[n_experts];
-  const long long total = nslots * vec_per_row;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
-    const long long slot = i / vec_per_row;
-    const int v = (int)(i - slot * vec_per_row);
-    zp[i] = z[(long long)perm[slot] * vec_per_row + v];
+  const int nslots = offsets[n_experts];
+  const int lane = threadIdx.x & 31;
+  const int wpb = blockDim.x >> 5;
+  for (int slot = blockIdx.x * wpb + (threadIdx.x >> 5); slot < nslots; slot += gridDim.x * wpb) {
+    const uint4* src = z + (long long)perm[slot] * vec_per_row;
+    uint4* dst = zp + (long long)slot * vec_per_row;
+    for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
   }
 }
 

@@ -125,6 +125,7 @@ qb_cutoff_kernel(const float* __restrict__ logits_t, int bt, int n_experts, int 
 constexpr float kKeyTol = 1e-6f;
 constexpr double kTaken64 = -3.0;     // below every key (keys lie in [-1, 1])
 constexpr int kTopkMaxWarps = 8;
+constexpr int kRegKeys = 32;          // keys per lane held in registers (E <= 1024)
 constexpr size_t kTopkSmemCap = 96 * 1024;
 
 __device__ __forceinline__ bool topk_better(bool v1, double k1, int e1, bool v2, double k2, int e2) {
@@ -168,17 +169,40 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
 
   for (int t = blockIdx.x * nwarps + warp; t < bt; t += gridDim.x * nwarps) {
     const float* lrow = logits + (size_t)t * E;
-    // 1. fp32 keys
-    for (int e = lane; e < E; e += 32)
-      ku[e] = f32_to_key(1.0f / (1.0f + expf(-lrow[e])) - s_alpha32[e]);
+    // 1. fp32 keys (also kept in registers when every lane has at most kRegKeys of them)
+    uint32_t kr[kRegKeys];
+    if (E <= 32 * kRegKeys) {
+#pragma unroll
+      for (int i = 0; i < kRegKeys; ++i) {
+        const int e = lane + 32 * i;
+        kr[i] = 0u;
+        if (e < E) {
+          kr[i] = f32_to_key(1.0f / (1.0f + expf(-lrow[e])) - s_alpha32[e]);
+          ku[e] = kr[i];
+        }
+      }
+    } else {
+      for (int e = lane; e < E; e += 32) ku[e] = f32_to_key(1.0f / (1.0f + expf(-lrow[e])) - s_alpha32[e]);
+    }
     __syncwarp();
-    // 2. the K-th largest key: the largest v with at least K keys >= v
+    // 2. the K-th largest key: the largest v with at least K keys >= v (key 0 is below every
+    //    real key, so the register slots past E never count)
     uint32_t v = 0;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = v | (1u << bit);
-      uint32_t c = 0;
-      for (int e = lane; e < E; e += 32) c += ku[e] >= cand ? 1u : 0u;
-      if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)top_k) v = cand;
+    if (E <= 32 * kRegKeys) {
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = v | (1u << bit);
+        uint32_t c = 0;
+#pragma unroll
+        for (int i = 0; i < kRegKeys; ++i) c += kr[i] >= cand ? 1u : 0u;
+        if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)top_k) v = cand;
+      }
+    } else {
+      for (int bit = 31; bit >= 0; --bit) {
+        const uint32_t cand = v | (1u << bit);
+        uint32_t c = 0;
+        for (int e = lane; e < E; e += 32) c += ku[e] >= cand ? 1u : 0u;
+        if (__reduce_add_sync(0xffffffffu, c) >= (uint32_t)top_k) v = cand;
+      }
     }
     // 3. candidates
     const uint32_t thr = f32_to_key(key_to_f32(v) - 2.0f * kKeyTol);
