@@ -263,6 +263,84 @@ def dense_ffn(x: np.ndarray, w_gate, w_up, w_down, beta: float = 4.0, beta_u: fl
     return situ_glu(x @ _f64(w_gate).T, x @ _f64(w_up).T, beta, beta_u) @ _f64(w_down).T
 
 
+# --------------------------------------------------------------------------- fp8 experts
+#
+# [K3-news] ¶"第一": the bounded SiTU-GLU output is what makes fp8 inference possible.  The
+# fp8 variant of the routed experts (a next step beyond the bf16 layer) is read as:
+#   * expert weights in e4m3 with one fp32 scale per output row: s = absmax(row) / 448 (in
+#     fp32; 1 for an all-zero row), q = e4m3(row / s) (fp32 division, then rounding);
+#   * the experts' input z (as the layer stores it, bf16) quantized the same way per token;
+#   * the expert activation h quantized with one fixed scale from the SiTU-GLU bound
+#     beta * beta_u >= |act|: q = e4m3(act * r) with r = fp32(448 / (beta * beta_u)), read
+#     back as q * s_h with s_h = fp32(beta * beta_u / 448);
+#   * e4m3 rounding to nearest, ties to even, saturating at +-448 (no NaN from overflow).
+# Everything else (router, down/up projections, shared experts) stays as in the bf16 layer.
+
+E4M3_MAX = 448.0
+
+
+def round_e4m3(v) -> np.ndarray:
+    """Nearest e4m3 value (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+    infinities), ties to even, saturating at +-448; subnormal spacing 2^-9."""
+    v = np.asarray(v, np.float64)
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)                       # below 2^-6 the spacing stays 2^-9
+    quantum = np.exp2(e - 3.0)
+    q = np.round(a / quantum) * quantum           # np.round: half to even
+    q = np.minimum(q, E4M3_MAX)
+    return np.where(a > 0, np.copysign(q, v), 0.0 * v)
+
+
+def quantize_rows_e4m3(w) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row e4m3 quantization: returns (q, s) with q on the e4m3 grid (as float64) and s
+    the fp32 row scales, so that w ~= q * s (see the fp8 reading above)."""
+    w32 = np.asarray(w, np.float32)
+    amax = np.abs(w32).max(axis=-1)
+    s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
+    q = round_e4m3((w32 / s[..., None]).astype(np.float32))
+    return q, s
+
+
+def h_scales(beta: float, beta_u: float) -> tuple[np.float32, np.float32]:
+    """(r, s_h): the fixed activation scale of the fp8 experts from the SiTU-GLU bound."""
+    bound = np.float32(beta) * np.float32(beta_u)
+    return np.float32(E4M3_MAX) / bound, bound / np.float32(E4M3_MAX)
+
+
+def bf16_round(v) -> np.ndarray:
+    """Nearest bf16 value (ties to even) of fp32 values, as float64."""
+    u = np.asarray(v, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+    return r.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weights_fp8, gamma, beta: float,
+                      beta_u: float, eps: float) -> np.ndarray:
+    """routed_latent with fp8 experts: z (the bf16 values the layer stores) quantized per
+    token, expert weights given as (q, s) pairs per expert, h quantized with the fixed
+    scale, everything else in fp64."""
+    z = np.asarray(z_bf16, np.float64)
+    n, latent = z.shape
+    zq, zs = quantize_rows_e4m3(z)
+    zd = zq * zs[:, None].astype(np.float64)
+    r, s_h = h_scales(beta, beta_u)
+    c = np.zeros((n, latent))
+    gamma = _f64(gamma)
+    for e in np.unique(idx):
+        rows, ks = np.nonzero(idx == e)
+        (gq, gs), (uq, us), (dq, ds) = weights_fp8[int(e)]
+        wg = gq * np.asarray(gs, np.float64)[:, None]
+        wu = uq * np.asarray(us, np.float64)[:, None]
+        wd = dq * np.asarray(ds, np.float64)[:, None]
+        zr = zd[rows]
+        a = situ_glu(zr @ wg.T, zr @ wu.T, beta, beta_u)
+        hq = round_e4m3(a * np.float64(r)) * np.float64(s_h)
+        yhat = rms_norm(hq @ wd.T, gamma, eps)
+        c[rows] += _f64(w)[rows, ks][:, None] * yhat
+    return c
+
+
 def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float = 4.0,
                   beta_u: float = 25.0, eps: float = 1e-6, return_parts: bool = False):
     """Stable LatentMoE layer output for the rows of x, given their routing (idx, w).

@@ -106,3 +106,23 @@ def test_dense_ffn_swapped_gate_and_up_is_caught(monkeypatch):
     orig = O.dense_ffn
     monkeypatch.setattr(O, "dense_ffn", lambda x, wg, wu, wd, beta=4.0, beta_u=25.0: orig(x, wu, wg, wd, beta, beta_u))
     assert _fails(P.test_dense_ffn_matches_torch_library_formulation)
+
+
+def test_fp8_dropped_weight_scale_is_caught(monkeypatch):
+    orig = O.quantize_rows_e4m3
+    monkeypatch.setattr(O, "quantize_rows_e4m3", lambda w: (orig(w)[0], np.ones_like(orig(w)[1])))
+    assert _fails(P.test_fp8_routed_latent_is_close_to_bf16_one)
+
+
+def test_e4m3_round_half_away_is_caught(monkeypatch):
+    orig = O.round_e4m3
+
+    def half_away(v):
+        v = np.asarray(v, np.float64)
+        a = np.abs(v)
+        e = np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), -6.0)
+        qn = np.exp2(e - 3.0)
+        q = np.minimum(np.floor(a / qn + 0.5) * qn, 448.0)
+        return np.where(a > 0, np.copysign(q, v), 0.0 * v)
+    monkeypatch.setattr(O, "round_e4m3", half_away)
+    assert _fails(P.test_round_e4m3_matches_torch_float8)

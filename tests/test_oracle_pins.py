@@ -445,3 +445,65 @@ def test_dense_ffn_splits_over_the_intermediate_dimension():
     whole = O.dense_ffn(x, wg, wu, wd)
     parts = O.dense_ffn(x, wg[:h], wu[:h], wd[:, :h]) + O.dense_ffn(x, wg[h:], wu[h:], wd[:, h:])
     np.testing.assert_allclose(parts, whole, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------- fp8 experts
+
+def test_round_e4m3_matches_torch_float8():
+    """e4m3 rounding against torch's float8_e4m3fn conversion (a library routine) on values
+    inside its range (torch turns values above 464 into NaN; the oracle saturates)."""
+    rng = np.random.default_rng(11)
+    v = (rng.normal(size=50000) * 10.0 ** rng.integers(-4, 3, 50000)).astype(np.float32)
+    v = np.concatenate([v, np.array([0, 2 ** -10, 1.5 * 2 ** -10, 2 ** -11, 448, 464, 1.0625, 1.1875, -2 ** -9],
+                                    np.float32)])
+    v = v[np.abs(v) <= 464]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.round_e4m3(v), ref)
+
+
+def test_round_e4m3_saturates_and_has_256_codes():
+    np.testing.assert_array_equal(O.round_e4m3([500.0, -1e9, 470.0]), [448.0, -448.0, 448.0])
+    # every finite e4m3 code (bit patterns from torch) is a fixed point
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    codes = codes[np.isfinite(codes)]
+    assert codes.size == 254
+    np.testing.assert_array_equal(O.round_e4m3(codes), codes)
+
+
+def test_bf16_round_matches_torch():
+    x = np.random.default_rng(12).normal(size=10000).astype(np.float32) * np.float32(3.7)
+    np.testing.assert_array_equal(O.bf16_round(x), torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy())
+
+
+def test_quantize_rows_e4m3_error_bound():
+    """Each row's largest element maps to +-448, and the reconstruction error of an element
+    of magnitude >= 2^-6 s is at most half an e4m3 step (2^-4 relative); zero rows stay zero."""
+    rng = np.random.default_rng(13)
+    w = rng.normal(size=(64, 96)).astype(np.float32) * np.float32(0.03)
+    w[5] = 0.0
+    q, s = O.quantize_rows_e4m3(w)
+    assert np.all(np.abs(q[np.arange(64) != 5]).max(axis=1) == 448.0)
+    assert np.all(q[5] == 0) and s[5] == 1.0
+    rec = q * s[:, None].astype(np.float64)
+    big = np.abs(w) >= 2.0 ** -6 * s[:, None]
+    assert np.all(np.abs(rec - w)[big] <= 2.0 ** -4 * np.abs(w)[big] + 1e-12)
+
+
+def test_fp8_routed_latent_is_close_to_bf16_one():
+    """The fp8 experts change the routed latent by e4m3 rounding only: within a few percent
+    (relative L2) of the unquantized path on the small recipe, and the fixed activation
+    scale never saturates (|act| < beta * beta_u)."""
+    w = WORKLOADS["small_bf16"]
+    s = w.shape
+    x, weights, _ = make_inputs(w, "cpu", 48)
+    W = _weights_np(weights)
+    z = O.bf16_round((_np(x) @ W["w_down"].T).astype(np.float32))
+    r = O.route(O.router_logits(_np(x), W["w_router"]), s.top_k)
+    ref = O.routed_latent(z, r["idx"], r["w"], W, s.beta, s.beta_u, s.rms_eps)
+    fp8 = {e: (O.quantize_rows_e4m3(W["exp_gate"][e]), O.quantize_rows_e4m3(W["exp_up"][e]),
+               O.quantize_rows_e4m3(W["exp_down"][e])) for e in range(s.n_experts)}
+    got = O.routed_latent_fp8(z, r["idx"], r["w"], fp8, W["latent_gamma"], s.beta, s.beta_u, s.rms_eps)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    assert 1e-3 < rel < 0.08, rel
+    rh, sh = O.h_scales(s.beta, s.beta_u)
+    assert float(rh) * s.beta * s.beta_u <= 448.0 * (1 + 1e-6) and abs(float(rh) * float(sh) - 1.0) < 1e-6
