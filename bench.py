@@ -37,13 +37,29 @@ METRIC = "LatentMoE layer fwd tokens/s on 1 B300; % of bf16 TC peak (or HBM BW)"
 
 # ----------------------------------------------------------------------------- arithmetic
 
-def algorithmic(shape, bt, n_touched):
+def algorithmic(shape, bt, n_touched, fp8_experts=False):
     """Algorithmic FLOPs and bytes of one layer call and of each stage (2*M*N*K per GEMM;
     bytes = what each stage must read and write at least once).  n_touched = experts
-    with at least one token."""
+    with at least one token.  With fp8 experts their weights, token rows and activations
+    are one byte per value (plus 4-byte row scales)."""
     d, L, E, K, I, S, Is = (shape.d, shape.latent, shape.n_experts, shape.top_k, shape.expert_inter,
                             shape.n_shared, shape.shared_inter)
     b = 2 if shape.dtype == "bf16" else 4
+    if fp8_experts:
+        st = {
+            "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
+            "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
+            "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
+            "expert_gate_up_gemm": (2 * bt * K * 2 * I * L,
+                                    n_touched * 2 * I * (L + 4) + bt * K * (L + 4) + bt * K * I),
+            "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * (I + 4) + bt * K * I + bt * K * L * b),
+            "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),
+            "shared_gate_up_gemm": (2 * bt * S * 2 * Is * d, (S * 2 * Is * d + bt * d + bt * S * Is) * b),
+            "up_shared_down_gemm": (2 * bt * d * (L + S * Is), (d * (L + S * Is) + bt * (L + S * Is) + bt * d) * b),
+        }
+        flops = 2 * bt * (E * d + L * d + K * 3 * L * I + d * L + S * 3 * d * Is)
+        weight_bytes = (E * d + 2 * L * d + L + S * 3 * d * Is) * b + n_touched * 3 * L * I + n_touched * (2 * I + L) * 4
+        return flops, weight_bytes + 2 * bt * d * b, st
     st = {
         "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
         "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
@@ -353,6 +369,8 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens-ref", type=int, default=2, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--fp8-experts", action="store_true",
+                    help="routed experts in e4m3 (lmoe_create_fp8); a separate line, not the bf16 headline")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -373,7 +391,15 @@ def main(argv=None):
     s = w.shape
     x, weights, bias = make_inputs(w, device)
     xs = [x, make_x(w, device, seed_offset=1 + rank)]
-    layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias)
+    if args.fp8_experts:
+        from sparse_moe_layer_cutoff_b300.lmoe import quantize_experts_fp8
+        f8 = quantize_experts_fp8(weights)
+        for n in ("exp_gate", "exp_up", "exp_down"):
+            del weights[n]
+        torch.cuda.empty_cache()
+        layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias, fp8_experts=f8)
+    else:
+        layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias)
     out = torch.empty((w.bt, s.d), dtype=layer.dtype, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -415,7 +441,7 @@ def main(argv=None):
 
     # ---- roofline of the dominant kernel (largest share of the timed region)
     pk = peaks()
-    flops, layer_bytes, per_stage = algorithmic(s, w.bt, n_touched)
+    flops, layer_bytes, per_stage = algorithmic(s, w.bt, n_touched, fp8_experts=args.fp8_experts)
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     dom_ms = stage_ms[dom] / max(calls, 1)
     f, b = per_stage[dom]
@@ -460,7 +486,7 @@ def main(argv=None):
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.fp8_experts:
         t = oracle_sample_time(w, x, weights, bias, args.cpu_tokens)
         cpu = {"value": args.cpu_tokens / t, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{args.cpu_tokens} tokens spread over the batch, routed among themselves, "
@@ -482,6 +508,9 @@ def main(argv=None):
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
                         "d2h_bytes_per_step": xbytes},
                 "gpu_launches": launches, "clocks": clk, "engine": lmoe_build_info()}
+        if args.fp8_experts:
+            line["dtype"] = "bf16 (routed experts e4m3)"
+            line["metric"] = METRIC + " [fp8 routed experts]"
         print(json.dumps(line), flush=True)
     layer.close()
     if ws > 1:

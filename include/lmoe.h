@@ -213,6 +213,42 @@ LMOE_API lmoe_status lmoe_segments_noalloc(const int32_t* topk_idx, int32_t bt, 
                                            int32_t* perm, int32_t* inv, lmoe_stream stream);
 
 /* ---------------------------------------------------------------------------------------
+ * fp8 (e4m3) routed experts ("KimiK3的StableLatentMoE架构解析", ¶"第一": the bounded SiTU-GLU
+ * output is what makes fp8 inference possible).  The routed experts' weights are e4m3 with
+ * one fp32 scale per output row; the experts' input z is quantized per token and their
+ * activation with one fixed scale from the SiTU-GLU bound (|act| < beta * beta_u):
+ *   row quantization: s = absmax / 448 (fp32; 1 for an all-zero row), q = e4m3(x * (1 / s)),
+ *                     e4m3 rounding to nearest, ties to even, saturating at +-448;
+ *   activation:       q = e4m3(act * (448 / (beta * beta_u))).
+ * Router, W_down, W_up and the shared experts stay bf16; the expert GEMMs run as tcgen05
+ * kind::f8f6f4 (e4m3 x e4m3 -> fp32).
+ * --------------------------------------------------------------------------------------- */
+typedef struct {
+  const void* exp_gate;      /* e4m3 bytes [E, I, L] (16-byte aligned)                      */
+  const void* exp_up;        /* e4m3 bytes [E, I, L]                                         */
+  const void* exp_down;      /* e4m3 bytes [E, L, I]                                         */
+  const float* gate_scale;   /* [E * I] fp32 row scales of exp_gate                          */
+  const float* up_scale;     /* [E * I]                                                      */
+  const float* down_scale;   /* [E * L]                                                      */
+} lmoe_fp8_experts;
+
+/* As lmoe_create (cfg->dtype must be LMOE_BF16), with the routed experts taken from
+ * `experts` (borrowed device buffers, as produced by lmoe_quantize_fp8_rows); w's exp_gate,
+ * exp_up and exp_down are not used and may be NULL.  lmoe_route / lmoe_forward /
+ * lmoe_destroy work unchanged; in lmoe_workspace's view, h holds the e4m3 activations
+ * (bytes).  LMOE_ERR_UNSUPPORTED if the tensor-core engine is disabled (LMOE_FORCE_SIMT). */
+LMOE_API lmoe_status lmoe_create_fp8(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* experts,
+                                     int32_t max_bt, lmoe_stream stream, lmoe_ctx** out);
+
+/* Row quantization to e4m3 as described above: w [rows, cols] bf16 (device, 16-byte
+ * aligned, cols a multiple of 8) -> q [rows, cols] e4m3 bytes (8-byte aligned) and
+ * scale [rows] fp32, on `stream`.  rows == 0 does nothing; bad pointers or sizes give
+ * LMOE_ERR_INVALID_ARG, cols not a multiple of 8 LMOE_ERR_UNSUPPORTED.  Expert weights
+ * [E, R, C] are quantized as E * R rows of C. */
+LMOE_API lmoe_status lmoe_quantize_fp8_rows(const void* w, int64_t rows, int32_t cols, void* q, float* scale,
+                                            lmoe_stream stream);
+
+/* ---------------------------------------------------------------------------------------
  * Dense SiTU-GLU FFN: the full-width feed-forward block of the model's first (dense) layer
  * ("Vue d'ensemble de l'architecture", mkdocs.reaper.mx, table "Le budget de paramètres,
  * module par module": 727 M parameters, intermediate 33 792 at d = 7168), with the experts'

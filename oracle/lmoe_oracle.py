@@ -268,7 +268,8 @@ def dense_ffn(x: np.ndarray, w_gate, w_up, w_down, beta: float = 4.0, beta_u: fl
 # [K3-news] ¶"第一": the bounded SiTU-GLU output is what makes fp8 inference possible.  The
 # fp8 variant of the routed experts (a next step beyond the bf16 layer) is read as:
 #   * expert weights in e4m3 with one fp32 scale per output row: s = absmax(row) / 448 (in
-#     fp32; 1 for an all-zero row), q = e4m3(row / s) (fp32 division, then rounding);
+#     fp32; 1 for an all-zero row), q = e4m3(row * (1 / s)) (the reciprocal and the product
+#     each rounded to fp32, then e4m3 rounding);
 #   * the experts' input z (as the layer stores it, bf16) quantized the same way per token;
 #   * the expert activation h quantized with one fixed scale from the SiTU-GLU bound
 #     beta * beta_u >= |act|: q = e4m3(act * r) with r = fp32(448 / (beta * beta_u)), read
@@ -298,7 +299,8 @@ def quantize_rows_e4m3(w) -> tuple[np.ndarray, np.ndarray]:
     w32 = np.asarray(w, np.float32)
     amax = np.abs(w32).max(axis=-1)
     s = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
-    q = round_e4m3((w32 / s[..., None]).astype(np.float32))
+    inv = (np.float32(1.0) / s).astype(np.float32)
+    q = round_e4m3((w32 * inv[..., None]).astype(np.float32))
     return q, s
 
 
@@ -339,6 +341,20 @@ def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weight
         yhat = rms_norm(hq @ wd.T, gamma, eps)
         c[rows] += _f64(w)[rows, ks][:, None] * yhat
     return c
+
+
+def layer_forward_fp8(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, weights_fp8, beta: float = 4.0,
+                      beta_u: float = 25.0, eps: float = 1e-6, z_bf16: np.ndarray | None = None) -> np.ndarray:
+    """Layer output with fp8 routed experts (see the fp8 reading above): z = x W_down^T is
+    rounded to bf16 as the layer stores it, the routed latent uses routed_latent_fp8, and the
+    up projection and shared experts are as in layer_forward.  weights_fp8[e] holds the
+    (q, s) pairs of expert e's gate, up and down weights.  z_bf16, if given, is used as the
+    stored z (the per-token scale is a discontinuous function of z, so parity checks take
+    the same stored values on both sides, as routing takes the same logits)."""
+    x = _f64(x)
+    z = bf16_round((x @ _f64(weights["w_down"]).T).astype(np.float32)) if z_bf16 is None else _f64(z_bf16)
+    c = routed_latent_fp8(z, idx, w, weights_fp8, weights["latent_gamma"], beta, beta_u, eps)
+    return c @ _f64(weights["w_up"]).T + shared_experts(x, weights, beta, beta_u)
 
 
 def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float = 4.0,

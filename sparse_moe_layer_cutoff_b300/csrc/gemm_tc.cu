@@ -28,6 +28,7 @@
 // bounded: on expiry the kernel records the timeout status, drains what it issued and
 // returns.
 #include <cuda.h>
+#include <cuda_fp8.h>
 
 #include <cstring>
 #include <new>
@@ -91,6 +92,13 @@ struct TcParams {
   const float* bias;
   float beta, beta_u;
   float inv_beta, inv_beta_u;
+  // fp8 (e4m3) routed experts: acc * wscale[row] * tscale[slot] is the gate / up value (GLU,
+  // up rows scaled by wscale_up), h is stored as e4m3(act * h_mul); the store kind writes
+  // acc * wscale[row] * out_mul
+  const float* wscale;
+  const float* wscale_up;
+  const float* tscale;
+  float h_mul, out_mul;
   uint32_t* status;
 };
 
@@ -192,15 +200,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// kind::f8f6f4 (both operands e4m3, fp32 accumulator): 32 K-elements (32 bytes) per call.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
+      : "memory");
+}
+template <bool F8>
+__device__ __forceinline__ void tc_mma_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  if (F8) tc_mma_f8(d, a, b, idesc, acc);
+  else tc_mma(d, a, b, idesc, acc);
+}
+
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of 128 bytes
 // in 8-row (1024-byte) groups; start address advanced by 32 bytes per K step of 16.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 accumulator.
+// Instruction descriptor: fp32 accumulator, A and B K-major; A / B format 1 = bf16 under
+// kind::f16, 0 = e4m3 under kind::f8f6f4.
 __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t idesc_e4m3(int m, int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
 
 // tanh by the MUFU hardware approximation (PTX tanh.approx.f32).
@@ -222,6 +248,11 @@ __device__ __forceinline__ float situ_glu_fast(float g, float u, const P& p) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// fp32 -> e4m3 (nearest, ties to even, saturating at +-448).
+__device__ __forceinline__ uint8_t e4m3_byte(float v) {
+  return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
 
 // Barrier over the epilogue warps that also ORs a flag across them.
@@ -305,9 +336,10 @@ __device__ __forceinline__ uint32_t acc_col(bool wide, int slot, int h) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int EPI>
+template <int EPI, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  constexpr int kBKe = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -361,7 +393,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     // ---------------------------------------------------------------- weight producer
     // Weight operand h of k-block kb of a tile: tensor map and coordinates.
     auto w_src = [&](const Tile& tl, int kb, int h, const CUtensorMap*& m, int& x, int& y) {
-      const int k = kb * kBK;
+      const int k = kb * kBKe;
       if (EPI == kEpiGlu) {
         m = h ? &maps.wup : &maps.w[0];
         x = k;
@@ -427,7 +459,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         __syncwarp();
         const uint32_t dst = tbase + stage * kTStageBytes;
         if (lane < nbox)
-          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, k_rot(p, tl, kb) * kBK, tl.tok0 + lane * kTokBox,
+          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, k_rot(p, tl, kb) * kBKe, tl.tok0 + lane * kTokBox,
                       tfull_bar(stage), tpol);
         pending |= 1u << stage;
         pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
@@ -451,7 +483,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int ntr = (tl.ntok + 15) & ~15;
         const bool wide = ntr > kHalf;
         const int nh = tile_halves<EPI>(p, tl);
-        const uint32_t idesc = idesc_bf16(kHalf, ntr);
+        const uint32_t idesc = F8 ? idesc_e4m3(kHalf, ntr) : idesc_bf16(kHalf, ntr);
         if (wide) {
           if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status) ||
               !mbar_wait(aempty_bar(1), aph[1] ^ 1u, abort_flag, p.status)) { stop = true; break; }
@@ -469,12 +501,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const uint64_t bd = smem_desc(tbase + ts * kTStageBytes);
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)
-            tc_mma(d0, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+            tc_mma_k<F8>(d0, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
           if (nh == 2) {
             const uint64_t ad1 = ad + (uint64_t)(kHalfBytes >> 4);
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j)
-              tc_mma(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+              tc_mma_k<F8>(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
           }
           issued = true;
           tc_commit(wempty_bar(ws));
@@ -525,6 +557,15 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       // tokens; TMEM is released before they are written out.
       uint32_t res[kMaxChunks][2][16];
       if (EPI == kEpiGlu) {
+        // fp8: per-row weight scales of this lane's feature (gate and up rows)
+        float sg = 1.f, su = 1.f;
+        if (F8) {
+          const int fo = tl.fb * kHalf + q * 32 + lane;
+          if (fo < p.n_feat) {
+            sg = p.wscale[(long long)tl.g * p.w_group_rows + fo];
+            su = p.wscale_up[(long long)tl.g * p.w_group_rows + fo];
+          }
+        }
 #pragma unroll
         for (int ci = 0; ci < kMaxChunks; ++ci) {
           const int c = sub + 3 * ci;
@@ -532,11 +573,28 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
             uint32_t g[32], u[32];
             tmem_ld32(c0 + c * 32, g);
             tmem_ld32(c1 + c * 32, u);
+            float ts = 1.f;   // fp8: this lane's token scale (lane j holds token j of the chunk)
+            if (F8 && c * 32 + lane < tl.ntok) ts = p.tscale[tl.tok0 + c * 32 + lane];
             tmem_wait_ld();
+            if (F8) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              res[ci][0][j] = pack_bf16x2(situ_glu_fast(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]), p),
-                                          situ_glu_fast(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]), p));
+              for (int j = 0; j < 32; j += 4) {
+                uint32_t word = 0;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                  const float tj = __shfl_sync(0xffffffffu, ts, j + b);
+                  const float a = situ_glu_fast(__uint_as_float(g[j + b]) * (sg * tj),
+                                                __uint_as_float(u[j + b]) * (su * tj), p);
+                  word |= (uint32_t)e4m3_byte(a * p.h_mul) << (8 * b);
+                }
+                res[ci][0][j >> 2] = word;
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                res[ci][0][j] = pack_bf16x2(situ_glu_fast(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]), p),
+                                            situ_glu_fast(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]), p));
+            }
           }
         }
       } else if (EPI == kEpiStore) {
@@ -549,10 +607,15 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               if (h < nh) {
                 uint32_t v[32];
                 tmem_ld32((h ? c1 : c0) + c * 32, v);
+                float sc = 1.f;   // fp8: row scale times the activation scale
+                if (F8) {
+                  const int fo = tl.fb * 2 * kHalf + h * kHalf + q * 32 + lane;
+                  if (fo < p.n_feat) sc = p.wscale[(long long)tl.g * p.w_group_rows + fo] * p.out_mul;
+                }
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                  res[ci][h][j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+                  res[ci][h][j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sc, __uint_as_float(v[2 * j + 1]) * sc);
               }
             }
           }
@@ -607,13 +670,20 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           for (int h = 0; h < (EPI == kEpiGlu ? 1 : 2); ++h) {
             const int fout = fbase + h * kHalf;
             if (h >= nh || fout >= p.n_feat) continue;
-            bf16* o = static_cast<bf16*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
+            if (F8 && EPI == kEpiGlu) {
+              uint8_t* o = static_cast<uint8_t*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nj) {
-                const uint32_t w2 = res[ci][h][j >> 1];
-                o[(long long)j * p.ldo] = __ushort_as_bfloat16((unsigned short)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu)));
-              }
+              for (int j = 0; j < 32; ++j)
+                if (j < nj) o[(long long)j * p.ldo] = (uint8_t)(res[ci][0][j >> 2] >> (8 * (j & 3)));
+            } else {
+              bf16* o = static_cast<bf16*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j < nj) {
+                  const uint32_t w2 = res[ci][h][j >> 1];
+                  o[(long long)j * p.ldo] = __ushort_as_bfloat16((unsigned short)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu)));
+                }
+            }
           }
         }
       }
@@ -661,16 +731,19 @@ EncodeTiledFn encoder() {
   return fn;
 }
 
-// 2-D bf16 map over rows x cols (row stride ld elements), box 64 columns x box_rows rows,
-// 128-byte swizzle; rows past the end read as zero.
-bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_rows) {
+// 2-D map over rows x cols (row stride ld elements) of bf16 (box 64 columns) or of bytes
+// (e4m3, box 128 columns), box_rows rows, 128-byte swizzle; rows past the end read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, long long ld, int box_rows,
+              bool u8 = false) {
   EncodeTiledFn enc = encoder();
   if (!enc || rows <= 0) return false;
+  const int esz = u8 ? 1 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * esz};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esz), (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  return enc(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+             dims, strides, box, es,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -692,7 +765,7 @@ int dense_tok_tile(int bt, int n_fb, int grid) {
 }
 
 // One launch of the persistent kernel: grid = SMs (fewer when a dense GEMM has fewer tiles).
-cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st) {
+cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st, bool f8 = false) {
   if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, sm_count);
   int grid = sm_count;
   if (p.G == 0) {
@@ -700,6 +773,11 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
     if (tiles < grid) grid = (int)tiles;
   }
   if (grid <= 0) return cudaSuccess;
+  if (f8) {
+    if (epi == kEpiGlu) tc_gemm_kernel<kEpiGlu, true><<<grid, kThreads, kSmemBytes, st>>>(maps, p);
+    else tc_gemm_kernel<kEpiStore, true><<<grid, kThreads, kSmemBytes, st>>>(maps, p);
+    return cudaGetLastError();
+  }
   switch (epi) {
     case kEpiStore: tc_gemm_kernel<kEpiStore><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
     case kEpiGlu: tc_gemm_kernel<kEpiGlu><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
@@ -715,12 +793,16 @@ struct TcPlan {
   int max_bt;
   int sm_count;
   TcBuffers buf;
+  bool f8;                                                  // e4m3 routed experts
+  CUtensorMap m_gate8, m_up8, m_edown8, m_zq8, m_h8;        // their weights, token rows, h
+  const float *s_gate, *s_up, *s_down;                      // per-row weight scales
+  float h_mul, h_scale;                                     // fixed activation scale (SiTU-GLU bound)
   CUtensorMap m_router, m_down, m_gate, m_up, m_edown, m_shg, m_shu, m_wup, m_shd;  // weights
   CUtensorMap m_zp, m_h, m_cat;                                                       // workspace
 };
 
-lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int max_bt, int sm_count,
-                           const TcBuffers& buf, TcPlan** plan) {
+lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int max_bt,
+                           int sm_count, const TcBuffers& buf, TcPlan** plan) {
   *plan = nullptr;
   TcPlan* pl = new (std::nothrow) TcPlan();
   if (!pl) return LMOE_ERR_OOM;
@@ -732,9 +814,24 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int ma
   const long long E = c.n_experts, d = c.d, L = c.latent, I = c.expert_inter, S = c.n_shared, Is = c.shared_inter;
   const long long ldc = L + S * Is;
   const long long slots = (long long)max_bt * c.top_k;
-  bool ok = make_map(&pl->m_router, w->w_router, E, d, d, kHalf) && make_map(&pl->m_down, w->w_down, L, d, d, kHalf) &&
-            make_map(&pl->m_gate, w->exp_gate, E * I, L, L, kHalf) && make_map(&pl->m_up, w->exp_up, E * I, L, L, kHalf) &&
-            make_map(&pl->m_edown, w->exp_down, E * L, I, I, kHalf) &&
+  pl->f8 = f8 != nullptr;
+  bool ok = make_map(&pl->m_router, w->w_router, E, d, d, kHalf) && make_map(&pl->m_down, w->w_down, L, d, d, kHalf);
+  if (pl->f8) {
+    ok = ok && make_map(&pl->m_gate8, f8->exp_gate, E * I, L, L, kHalf, true) &&
+         make_map(&pl->m_up8, f8->exp_up, E * I, L, L, kHalf, true) &&
+         make_map(&pl->m_edown8, f8->exp_down, E * L, I, I, kHalf, true) &&
+         make_map(&pl->m_zq8, buf.zp, slots, L, L, kTokBox, true) && make_map(&pl->m_h8, buf.h, slots, I, I, kTokBox, true);
+    pl->s_gate = f8->gate_scale;
+    pl->s_up = f8->up_scale;
+    pl->s_down = f8->down_scale;
+    const float bound = c.beta * c.beta_u;   // |SiTU-GLU| < beta * beta_u
+    pl->h_mul = 448.0f / bound;
+    pl->h_scale = bound / 448.0f;
+  } else {
+    ok = ok && make_map(&pl->m_gate, w->exp_gate, E * I, L, L, kHalf) && make_map(&pl->m_up, w->exp_up, E * I, L, L, kHalf) &&
+         make_map(&pl->m_edown, w->exp_down, E * L, I, I, kHalf);
+  }
+  ok = ok &&
             make_map(&pl->m_shg, w->sh_gate, S * Is, d, d, kHalf) && make_map(&pl->m_shu, w->sh_up, S * Is, d, d, kHalf) &&
             make_map(&pl->m_wup, w->w_up, d, L, L, kHalf) && make_map(&pl->m_shd, w->sh_down, S * d, Is, Is, kHalf) &&
             make_map(&pl->m_zp, buf.zp, slots, L, L, kTokBox) && make_map(&pl->m_h, buf.h, slots, I, I, kTokBox) &&
@@ -748,6 +845,10 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int ma
     e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiRouter>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && pl->f8)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess && pl->f8)
+    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiStore, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) {
     cudaGetLastError();
     delete pl;
@@ -781,7 +882,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   p.status = pl->buf.status;
   p.tok_tile = kTokMax;
   int epi = a.epi;
-  bool ok = true;
+  bool ok = true, f8 = false;
   switch (a.op) {
     case kOpRouter:
       maps.w[0] = pl->m_router;
@@ -815,6 +916,26 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
       p.seg_k0[a.nseg] = a.K;
       break;
     case kOpExpertGateUp: {
+      if (pl->f8) {
+        // token rows of each expert segment, quantized per token into slot order
+        cudaError_t e = launch_gather_quant(pl->buf.z, a.a_rows, a.seg_off, a.G, c.latent, pl->buf.zp, pl->buf.tscale,
+                                            pl->sm_count * 8, st);
+        if (e != cudaSuccess) return e;
+        maps.w[0] = pl->m_gate8;
+        maps.wup = pl->m_up8;
+        maps.tok = pl->m_zq8;
+        p.wscale = pl->s_gate;
+        p.wscale_up = pl->s_up;
+        p.tscale = pl->buf.tscale;
+        p.h_mul = pl->h_mul;
+        p.w_group_rows = c.expert_inter;
+        p.seg_off = a.seg_off;
+        p.mtile_off = a.mtile_off;
+        p.G = a.G;
+        p.kblocks = a.K / (2 * kBK);
+        f8 = true;
+        break;
+      }
       // token rows of each expert segment, gathered once into slot order
       const int vec = c.latent / 8;
       gather_rows_kernel<<<pl->sm_count * 8, 256, 0, st>>>(static_cast<const uint4*>(pl->buf.z), a.a_rows, a.seg_off,
@@ -829,8 +950,17 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
       break;
     }
     case kOpExpertDown:
-      maps.w[0] = pl->m_edown;
-      maps.tok = pl->m_h;
+      if (pl->f8) {
+        maps.w[0] = pl->m_edown8;
+        maps.tok = pl->m_h8;
+        p.wscale = pl->s_down;
+        p.out_mul = pl->h_scale;
+        p.kblocks = a.K / (2 * kBK);
+        f8 = true;
+      } else {
+        maps.w[0] = pl->m_edown;
+        maps.tok = pl->m_h;
+      }
       p.w_group_rows = c.latent;
       p.seg_off = a.seg_off;
       p.mtile_off = a.mtile_off;
@@ -841,7 +971,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   }
   if (!ok) return cudaErrorInvalidValue;
   p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
-  return launch_tc(maps, p, epi, pl->sm_count, st);
+  return launch_tc(maps, p, epi, pl->sm_count, st, f8);
 }
 
 // ------------------------------------------------------------------ dense SiTU-GLU FFN

@@ -14,13 +14,16 @@ struct TcBuffers {
   void* h;
   void* y;
   void* cat;
+  float* tscale;     // [max_bt * K] per-slot token scales (fp8 experts)
   uint32_t* status;
 };
 
 // Builds the weight / workspace descriptors.  *plan == nullptr with LMOE_OK means the
 // engine does not cover this configuration.
-lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, int max_bt, int sm_count,
-                           const TcBuffers& buf, TcPlan** plan);
+// f8 != nullptr: routed experts in e4m3 (w's expert pointers are not used); zp and h then
+// hold e4m3 bytes.
+lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int max_bt,
+                           int sm_count, const TcBuffers& buf, TcPlan** plan);
 void tc_plan_destroy(TcPlan* plan);
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
 int tc_launches(int op);   // kernels launch_gemm_tc starts for one GemmOp

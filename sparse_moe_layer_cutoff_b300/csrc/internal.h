@@ -78,6 +78,10 @@ struct GemmArgs {
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, bool is_bf16, cudaStream_t st);
 
+// fp8 experts: zq[slot] = e4m3 rows of z[perm[slot]] with per-slot scales (csrc/fp8.cu).
+cudaError_t launch_gather_quant(const void* z, const int32_t* perm, const int32_t* offsets, int n_experts, int latent,
+                                void* zq, float* tscale, int grid, cudaStream_t st);
+
 // ---------------------------------------------------------------------------- combine
 struct CombineArgs {
   const void* y;          // [bt*K, L] slot-ordered expert outputs

@@ -49,6 +49,7 @@ struct lmoe_ctx {
   void* h;
   void* y;
   void* cat;
+  float* tscale;
   uint32_t* status;
   TcPlan* tc;
   // per-stage profiling
@@ -192,7 +193,12 @@ const char* lmoe_build_info(void) {
   return "lmoe sm_103a: bf16 = tcgen05/TMEM/TMA GEMMs, fp32 = CUDA-core fp32 FMA GEMMs";
 }
 
-lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt,
+}  // extern "C"
+
+namespace {
+
+// lmoe_create and lmoe_create_fp8 (f8 != nullptr: e4m3 routed experts).
+lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int32_t max_bt,
                         lmoe_stream stream, lmoe_ctx** out) {
   if (!out) return LMOE_ERR_INVALID_ARG;
   *out = nullptr;
@@ -201,15 +207,32 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   if (!w) return LMOE_ERR_INVALID_ARG;
   if (max_bt <= 0 || max_bt > (1 << 20)) return LMOE_ERR_INVALID_ARG;
   if ((long long)max_bt * cfg->top_k >= (1LL << 31)) return LMOE_ERR_UNSUPPORTED;
-  const void* req[] = {w->w_router, w->w_down, w->latent_gamma, w->w_up, w->exp_gate,
-                       w->exp_up, w->exp_down, w->sh_gate, w->sh_up, w->sh_down};
+  if (f8 && cfg->dtype != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
+  const void* req[] = {w->w_router, w->w_down, w->latent_gamma, w->w_up, w->sh_gate, w->sh_up, w->sh_down,
+                       f8 ? f8->exp_gate : w->exp_gate, f8 ? f8->exp_up : w->exp_up, f8 ? f8->exp_down : w->exp_down};
   for (const void* p : req)
     if (!p || !aligned16(p)) return LMOE_ERR_INVALID_ARG;
   if (w->router_bias && !aligned16(w->router_bias)) return LMOE_ERR_INVALID_ARG;
+  if (f8) {
+    const float* sc[] = {f8->gate_scale, f8->up_scale, f8->down_scale};
+    for (const float* p : sc)
+      if (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) return LMOE_ERR_INVALID_ARG;
+  }
   // from here on the CUDA runtime is needed
   for (const void* p : req)
     if ((s = check_device_ptr(p)) != LMOE_OK) return s;
   if (w->router_bias && (s = check_device_ptr(w->router_bias)) != LMOE_OK) return s;
+  if (f8) {
+    const void* sc[] = {f8->gate_scale, f8->up_scale, f8->down_scale};
+    for (const void* p : sc) {
+      cudaPointerAttributes at;
+      if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return LMOE_ERR_INVALID_ARG;
+      }
+      if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged) return LMOE_ERR_INVALID_ARG;
+    }
+  }
 
   lmoe_ctx* ctx = new (std::nothrow) lmoe_ctx();
   if (!ctx) return LMOE_ERR_OOM;
@@ -252,6 +275,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   size_t o_h = cv.take<char>(bt * K * c.expert_inter * ctx->esz);
   size_t o_y = cv.take<char>(bt * K * L * ctx->esz);
   size_t o_cat = cv.take<char>(bt * ldc * ctx->esz);
+  size_t o_tscale = cv.take<float>(bt * K);
   ctx->ws_bytes = cv.off;
   if (cudaMalloc(&ctx->ws, ctx->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -277,6 +301,7 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   ctx->h = b + o_h;
   ctx->y = b + o_y;
   ctx->cat = b + o_cat;
+  ctx->tscale = (float*)(b + o_tscale);
   if (cudaMemset(ctx->ws, 0, ctx->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(ctx->ws);
@@ -287,11 +312,17 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   ctx->tc = nullptr;
   if (ctx->bf16) {
     const char* force = getenv("LMOE_FORCE_SIMT");
+    if (f8 && force && force[0] == '1') {
+      cudaFree(ctx->ws);
+      delete ctx;
+      return LMOE_ERR_UNSUPPORTED;
+    }
     if (!(force && force[0] == '1')) {
       TcBuffers tb;
       tb.z = ctx->z; tb.zp = ctx->zp; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
+      tb.tscale = ctx->tscale;
       tb.status = ctx->status;
-      lmoe_status ts = tc_plan_create(&c, w, max_bt, ctx->sm_count, tb, &ctx->tc);
+      lmoe_status ts = tc_plan_create(&c, w, f8, max_bt, ctx->sm_count, tb, &ctx->tc);
       if (ts != LMOE_OK) {
         cudaFree(ctx->ws);
         delete ctx;
@@ -302,6 +333,24 @@ lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t m
   }
   *out = ctx;
   return LMOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt, lmoe_stream stream,
+                        lmoe_ctx** out) {
+  return create_impl(cfg, w, nullptr, max_bt, stream, out);
+}
+
+lmoe_status lmoe_create_fp8(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* experts,
+                            int32_t max_bt, lmoe_stream stream, lmoe_ctx** out) {
+  if (!experts) {
+    if (out) *out = nullptr;
+    return LMOE_ERR_INVALID_ARG;
+  }
+  return create_impl(cfg, w, experts, max_bt, stream, out);
 }
 
 lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream,

@@ -35,6 +35,10 @@ class lmoe_weights(ctypes.Structure):
                                     "exp_gate", "exp_up", "exp_down", "sh_gate", "sh_up", "sh_down")]
 
 
+class lmoe_fp8_experts(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("exp_gate", "exp_up", "exp_down", "gate_scale", "up_scale", "down_scale")]
+
+
 class lmoe_ffn_config(ctypes.Structure):
     _fields_ = [("d", c_i32), ("inter", c_i32), ("beta", c_f32), ("beta_u", c_f32)]
 
@@ -76,6 +80,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_status_string.restype = ctypes.c_char_p
     lib.lmoe_workspace.argtypes = [c_vp, ctypes.POINTER(lmoe_workspace_view)]
     lib.lmoe_workspace.restype = c_i32
+    lib.lmoe_create_fp8.argtypes = [ctypes.POINTER(lmoe_config), ctypes.POINTER(lmoe_weights),
+                                    ctypes.POINTER(lmoe_fp8_experts), c_i32, c_vp, ctypes.POINTER(c_vp)]
+    lib.lmoe_create_fp8.restype = c_i32
+    lib.lmoe_quantize_fp8_rows.argtypes = [c_vp, ctypes.c_int64, c_i32, c_vp, c_vp, c_vp]
+    lib.lmoe_quantize_fp8_rows.restype = c_i32
     lib.lmoe_ffn_create.argtypes = [ctypes.POINTER(lmoe_ffn_config), c_vp, c_vp, c_vp, c_i32, ctypes.POINTER(c_vp)]
     lib.lmoe_ffn_create.restype = c_i32
     lib.lmoe_ffn_forward.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
@@ -151,6 +160,43 @@ STAGE_NAMES = ("router_gemm", "cutoff_topk_segments", "w_down_gemm", "expert_gat
                "expert_down_gemm", "rmsnorm_combine", "shared_gate_up_gemm", "up_shared_down_gemm")
 
 
+def lmoe_create_fp8(cfg: lmoe_config, weights: lmoe_weights, experts: lmoe_fp8_experts, max_bt: int,
+                    stream: int = 0):
+    ctx = c_vp()
+    st = load_library().lmoe_create_fp8(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(experts), max_bt,
+                                        c_vp(stream), ctypes.byref(ctx))
+    return st, ctx.value
+
+
+def lmoe_quantize_fp8_rows(w: int, rows: int, cols: int, q: int, scale: int, stream: int = 0) -> int:
+    return load_library().lmoe_quantize_fp8_rows(c_vp(w), rows, cols, c_vp(q), c_vp(scale), c_vp(stream))
+
+
+def quantize_fp8_rows(w):
+    """e4m3 row quantization of a bf16 CUDA tensor [..., cols] by the library:
+    returns (q uint8 tensor of w's shape, scale fp32 tensor of w.shape[:-1])."""
+    import torch
+
+    if w.dtype != torch.bfloat16 or not w.is_contiguous():
+        raise ValueError("quantize_fp8_rows needs a contiguous bf16 tensor")
+    q = torch.empty(w.shape, dtype=torch.uint8, device=w.device)
+    sc = torch.empty(w.shape[:-1], dtype=torch.float32, device=w.device)
+    rows = w.numel() // w.shape[-1]
+    st = lmoe_quantize_fp8_rows(w.data_ptr(), rows, w.shape[-1], q.data_ptr(), sc.data_ptr(),
+                                torch.cuda.current_stream().cuda_stream)
+    if st != LMOE_OK:
+        raise LmoeError(st, "lmoe_quantize_fp8_rows")
+    return q, sc
+
+
+def quantize_experts_fp8(weights: dict) -> dict:
+    """The routed experts of a bf16 weight dict in e4m3 (the dict lmoe_create_fp8 takes)."""
+    out = {}
+    for n in ("exp_gate", "exp_up", "exp_down"):
+        out[n], out[n.replace("exp_", "") + "_scale"] = quantize_fp8_rows(weights[n])
+    return out
+
+
 def lmoe_ffn_create(cfg: lmoe_ffn_config, w_gate: int, w_up: int, w_down: int, max_bt: int):
     ffn = c_vp()
     st = load_library().lmoe_ffn_create(ctypes.byref(cfg), c_vp(w_gate), c_vp(w_up), c_vp(w_down), max_bt,
@@ -215,16 +261,20 @@ WEIGHT_NAMES = ("w_router", "w_down", "latent_gamma", "w_up", "exp_gate", "exp_u
 class LatentMoE:
     """One layer context over borrowed torch CUDA tensors."""
 
-    def __init__(self, shape, weights: dict, max_bt: int, router_bias=None, stream=None):
+    def __init__(self, shape, weights: dict, max_bt: int, router_bias=None, stream=None, fp8_experts=None):
+        """fp8_experts: optional dict from quantize_experts_fp8 (e4m3 routed experts); the
+        bf16 expert weights in `weights` are then not used and may be absent."""
         import torch
 
         self.shape = shape
         self.dtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
-        self._keep = dict(weights)
+        self._keep = (dict(weights), dict(fp8_experts or {}))
         self._bias = router_bias
         w = lmoe_weights()
         for n in WEIGHT_NAMES:
-            t = weights[n]
+            t = weights.get(n)
+            if t is None and fp8_experts is not None and n.startswith("exp_"):
+                continue
             if not t.is_contiguous():
                 raise ValueError(f"{n} must be contiguous")
             setattr(w, n, t.data_ptr())
@@ -232,9 +282,14 @@ class LatentMoE:
         self.cfg = make_config(shape)
         self.max_bt = max_bt
         s = torch.cuda.current_stream() if stream is None else stream
-        st, ctx = lmoe_create(self.cfg, w, max_bt, s.cuda_stream)
+        if fp8_experts is None:
+            st, ctx = lmoe_create(self.cfg, w, max_bt, s.cuda_stream)
+        else:
+            f8 = lmoe_fp8_experts(*(fp8_experts[n].data_ptr() for n in
+                                    ("exp_gate", "exp_up", "exp_down", "gate_scale", "up_scale", "down_scale")))
+            st, ctx = lmoe_create_fp8(self.cfg, w, f8, max_bt, s.cuda_stream)
         if st != LMOE_OK:
-            raise LmoeError(st, "lmoe_create")
+            raise LmoeError(st, "lmoe_create_fp8" if fp8_experts is not None else "lmoe_create")
         self.ctx = ctx
 
     def _stream(self, stream):
