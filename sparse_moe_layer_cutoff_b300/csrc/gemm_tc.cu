@@ -1,10 +1,11 @@
-// Tensor-core engine of the bf16 layer: one persistent, warp-specialised tcgen05 GEMM
-// kernel serves every contraction ("Stable LatentMoE": router, down_proj, GroupedExperts
-// gate/up + SiTU-GLU, expert down, shared experts, up_proj + shared down).
+// Tensor-core engine of the layer: one persistent, warp-specialised tcgen05 GEMM kernel
+// serves every contraction ("Stable LatentMoE": router, down_proj, GroupedExperts gate/up +
+// SiTU-GLU, expert down, shared experts, up_proj + shared down), and the dense first-layer
+// FFN.  Operands are bf16 (kind::f16), or e4m3 for the fp8 routed experts (kind::f8f6f4).
 //
 // Weight-stationary tiles.  A tile is 256 weight rows (two MMA operands A0, A1 of M = 128
 // rows each) against up to kTokMax tokens (the MMA's N side, shared by both MMAs), with K
-// stepped 64 at a time (one 128-byte swizzle row of bf16):
+// stepped one 128-byte swizzle row at a time (64 bf16 or 128 e4m3 values):
 //   * GLU tiles: A0 = 128 gate rows, A1 = the 128 up rows of the same output features, so
 //     one TMEM lane holds both branches of a feature and the SiTU-GLU epilogue needs no
 //     exchange between warps;
@@ -21,12 +22,12 @@
 // token tiles through a kTStages ring (TMA, mbarrier completion), warp 1 owns TMEM and
 // issues tcgen05.mma (one thread), warps 4-15 drain the accumulators with tcgen05.ld (three
 // warps per TMEM lane quadrant, taking every third 32-token chunk) and write the outputs.
-// While a wide tile drains, the next one cannot start, so the SiTU-GLU epilogue uses the
+// While a wide tile drains, the next one cannot start, so the epilogue packs its results
+// into registers and releases TMEM before the global stores, and SiTU-GLU uses the
 // hardware tanh approximation (relative error about 2^-11, below the bf16 rounding of its
-// output) to keep that gap short.  The
-// expert tile schedule is copied into shared memory once per CTA.  Every mbarrier wait is
-// bounded: on expiry the kernel records the timeout status, drains what it issued and
-// returns.
+// output).  The expert tile schedule is copied into shared memory once per CTA.  Every
+// mbarrier wait is bounded: on expiry the kernel records the timeout status, drains what it
+// issued and returns.
 #include <cuda.h>
 #include <cuda_fp8.h>
 
