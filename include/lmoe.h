@@ -178,6 +178,15 @@ LMOE_API lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* ou
  * context or m outside [0, 1); no GPU work. */
 LMOE_API lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum);
 
+/* Failure-detection test hook.  Arms the next lmoe_forward on this context so that its
+ * routed-expert gate/up kernel leaves its token stages unfilled and limits its device-side
+ * waits to 20 ms: the waits run out, the kernel records the timeout in the status word,
+ * finishes its in-flight copies and matrix operations, frees its tensor memory and returns
+ * (no trap, no hang).  That forward's output is unspecified; lmoe_sync_status then returns
+ * LMOE_ERR_TIMEOUT (and clears it) and later calls work normally.  LMOE_ERR_UNSUPPORTED on the
+ * CUDA-core engine (fp32 layers). */
+LMOE_API lmoe_status lmoe_debug_inject_wait_timeout(lmoe_ctx* ctx);
+
 /* Per-stage device timing.  lmoe_profile(ctx, 1) clears the record and starts recording
  * CUDA events on the call's stream at every stage boundary of each lmoe_forward (up to
  * 1024 calls); lmoe_profile(ctx, 0) stops.  lmoe_profile_read synchronises on the

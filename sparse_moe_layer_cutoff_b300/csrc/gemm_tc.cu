@@ -64,6 +64,7 @@ constexpr int kOffBars = kOffSched + 2 * kSchedMax * 4;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = 1024 + kOffMisc + 16;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
+constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
 static_assert(kTokMax % 16 == 0 && kTokMax <= 256, "MMA N limit");
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 
@@ -100,6 +101,8 @@ struct TcParams {
   const float* wscale_up;
   const float* tscale;
   float h_mul, out_mul;
+  unsigned long long timeout_ns;  // limit of every mbarrier wait
+  int inject;               // test hook: the token producer leaves its stages unfilled
   uint32_t* status;
 };
 
@@ -136,14 +139,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
 // Bounded wait.  Gives up when the deadline passes (setting abort + timeout status) or,
 // if honour_abort, as soon as another role has aborted.
 __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       uint32_t* status, bool honour_abort = true) {
+                                       uint32_t* status, unsigned long long limit_ns, bool honour_abort = true) {
   if (mbar_test(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_test(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (honour_abort && *abort_flag) return false;
-      if (global_ns() - t0 > kTimeoutNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeout);
         return false;
@@ -418,7 +421,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const Tile tl = decode_tile(p, seg, mt, t);
         const int nh = tile_halves<EPI>(p, tl);
         for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait(wempty_bar(stage), phase ^ 1u, abort_flag, p.status)) { stop = true; break; }
+          if (!mbar_wait(wempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           pending &= ~(1u << stage);
           mbar_expect_tx(wfull_bar(stage), (uint32_t)(nh * kHalfBytes));
           const uint32_t dst = wbase + stage * kWStageBytes;
@@ -436,7 +439,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       if (stop) {
         // no copy may still be landing in shared memory when the block exits
         for (int s = 0; s < kWStages; ++s)
-          if (pending & (1u << s)) mbar_wait(wfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, false);
+          if (pending & (1u << s)) mbar_wait(wfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, p.timeout_ns, false);
       }
     }
     __syncwarp();
@@ -452,10 +455,15 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const int nbox = ntr / kTokBox;
       for (int kb = 0; kb < p.kblocks; ++kb) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(tempty_bar(stage), phase ^ 1u, abort_flag, p.status);
+        if (lane == 0) ok = mbar_wait(tempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) { stop = true; break; }
         pending &= ~(1u << stage);
+        if (p.inject) {
+          // test hook: nothing fills this stage, so its consumer's bounded wait runs out
+          if (++stage == kTStages) { stage = 0; phase ^= 1u; }
+          continue;
+        }
         if (lane == 0) mbar_expect_tx(tfull_bar(stage), (uint32_t)ntr * (kBK * 2));
         __syncwarp();
         const uint32_t dst = tbase + stage * kTStageBytes;
@@ -469,7 +477,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     }
     if (stop && lane == 0) {
       for (int s = 0; s < kTStages; ++s)
-        if (pending & (1u << s)) mbar_wait(tfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, false);
+        if (pending & (1u << s)) mbar_wait(tfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, p.timeout_ns, false);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -486,17 +494,17 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int nh = tile_halves<EPI>(p, tl);
         const uint32_t idesc = F8 ? idesc_e4m3(kHalf, ntr) : idesc_bf16(kHalf, ntr);
         if (wide) {
-          if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status) ||
-              !mbar_wait(aempty_bar(1), aph[1] ^ 1u, abort_flag, p.status)) { stop = true; break; }
+          if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status, p.timeout_ns) ||
+              !mbar_wait(aempty_bar(1), aph[1] ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
         } else {
-          if (!mbar_wait(aempty_bar(slot), aph[slot] ^ 1u, abort_flag, p.status)) { stop = true; break; }
+          if (!mbar_wait(aempty_bar(slot), aph[slot] ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
         }
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc_col(wide, slot, 0);
         const uint32_t d1 = tmem_base + acc_col(wide, slot, 1);
         for (int kb = 0; kb < p.kblocks; ++kb) {
-          if (!mbar_wait(wfull_bar(ws), wph, abort_flag, p.status) ||
-              !mbar_wait(tfull_bar(ts), tph, abort_flag, p.status)) { stop = true; break; }
+          if (!mbar_wait(wfull_bar(ws), wph, abort_flag, p.status, p.timeout_ns) ||
+              !mbar_wait(tfull_bar(ts), tph, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           tc_fence_after();
           const uint64_t ad = smem_desc(wbase + ws * kWStageBytes);
           const uint64_t bd = smem_desc(tbase + ts * kTStageBytes);
@@ -529,7 +537,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       }
       if (stop && issued) {
         tc_commit(drain_bar);
-        mbar_wait(drain_bar, 0, abort_flag, p.status, false);
+        mbar_wait(drain_bar, 0, abort_flag, p.status, p.timeout_ns, false);
       }
     }
     __syncwarp();
@@ -546,9 +554,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const bool wide = ntr > kHalf;
       const int nh = tile_halves<EPI>(p, tl);
       bool ok;
-      if (wide) ok = mbar_wait(afull_bar(0), aph[0], abort_flag, p.status) &&
-                     mbar_wait(afull_bar(1), aph[1], abort_flag, p.status);
-      else ok = mbar_wait(afull_bar(slot), aph[slot], abort_flag, p.status);
+      if (wide) ok = mbar_wait(afull_bar(0), aph[0], abort_flag, p.status, p.timeout_ns) &&
+                     mbar_wait(afull_bar(1), aph[1], abort_flag, p.status, p.timeout_ns);
+      else ok = mbar_wait(afull_bar(slot), aph[slot], abort_flag, p.status, p.timeout_ns);
       if (named_sync_or(1, kEpiThreads, !ok || *abort_flag)) break;
       tc_fence_after();
       const uint32_t c0 = lane_base + acc_col(wide, slot, 0);
@@ -798,6 +806,7 @@ struct TcPlan {
   CUtensorMap m_gate8, m_up8, m_edown8, m_zq8, m_h8;        // their weights, token rows, h
   const float *s_gate, *s_up, *s_down;                      // per-row weight scales
   float h_mul, h_scale;                                     // fixed activation scale (SiTU-GLU bound)
+  bool inject;                                              // test hook armed for the next expert gate/up
   CUtensorMap m_router, m_down, m_gate, m_up, m_edown, m_shg, m_shu, m_wup, m_shd;  // weights
   CUtensorMap m_zp, m_h, m_cat;                                                       // workspace
 };
@@ -861,6 +870,8 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const 
 
 void tc_plan_destroy(TcPlan* plan) { delete plan; }
 
+void tc_inject_wait_timeout(TcPlan* plan) { plan->inject = true; }
+
 int tc_launches(int op) { return op == kOpExpertGateUp ? 2 : 1; }
 
 cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
@@ -881,6 +892,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   p.inv_beta = 1.0f / a.beta;
   p.inv_beta_u = 1.0f / a.beta_u;
   p.status = pl->buf.status;
+  p.timeout_ns = kTimeoutNs;
   p.tok_tile = kTokMax;
   int epi = a.epi;
   bool ok = true, f8 = false;
@@ -917,6 +929,11 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
       p.seg_k0[a.nseg] = a.K;
       break;
     case kOpExpertGateUp: {
+      if (pl->inject) {
+        p.inject = 1;
+        p.timeout_ns = kInjectTimeoutNs;
+        pl->inject = false;
+      }
       if (pl->f8) {
         // token rows of each expert segment, quantized per token into slot order
         cudaError_t e = launch_gather_quant(pl->buf.z, a.a_rows, a.seg_off, a.G, c.latent, pl->buf.zp, pl->buf.tscale,
@@ -1029,6 +1046,7 @@ cudaError_t tc_ffn_forward(TcFfnPlan* pl, const void* x, int bt, void* out, cuda
     p.inv_beta = 1.0f / pl->beta;
     p.inv_beta_u = 1.0f / pl->beta_u;
     p.status = pl->status;
+    p.timeout_ns = kTimeoutNs;
     if (pass == 0) {
       maps.w[0] = pl->m_gate;
       maps.wup = pl->m_up;

@@ -25,6 +25,10 @@ struct TcBuffers {
 lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int max_bt,
                            int sm_count, const TcBuffers& buf, TcPlan** plan);
 void tc_plan_destroy(TcPlan* plan);
+// Test hook: the next routed-expert gate/up launch leaves its token stages unfilled and
+// shortens its waits to 20 ms, so the kernel times out, records LMOE timeout status and
+// returns.
+void tc_inject_wait_timeout(TcPlan* plan);
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
 int tc_launches(int op);   // kernels launch_gemm_tc starts for one GemmOp
 

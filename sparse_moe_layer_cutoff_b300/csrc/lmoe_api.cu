@@ -476,6 +476,13 @@ lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum) {
   return LMOE_OK;
 }
 
+lmoe_status lmoe_debug_inject_wait_timeout(lmoe_ctx* ctx) {
+  if (!ctx) return LMOE_ERR_INVALID_ARG;
+  if (!ctx->use_tc) return LMOE_ERR_UNSUPPORTED;
+  tc_inject_wait_timeout(ctx->tc);
+  return LMOE_OK;
+}
+
 lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable) {
   if (!ctx) return LMOE_ERR_INVALID_ARG;
   if (enable && ctx->prof_ev.empty()) {

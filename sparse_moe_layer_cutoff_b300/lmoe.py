@@ -93,6 +93,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_ffn_sync_status.restype = c_i32
     lib.lmoe_ffn_destroy.argtypes = [c_vp]
     lib.lmoe_ffn_destroy.restype = None
+    lib.lmoe_debug_inject_wait_timeout.argtypes = [c_vp]
+    lib.lmoe_debug_inject_wait_timeout.restype = c_i32
     lib.lmoe_set_cutoff_momentum.argtypes = [c_vp, ctypes.c_double]
     lib.lmoe_set_cutoff_momentum.restype = c_i32
     lib.lmoe_profile.argtypes = [c_vp, c_i32]
@@ -214,6 +216,11 @@ def lmoe_ffn_sync_status(ffn, stream: int = 0) -> int:
 
 def lmoe_ffn_destroy(ffn) -> None:
     load_library().lmoe_ffn_destroy(c_vp(ffn))
+
+
+def lmoe_debug_inject_wait_timeout(ctx) -> int:
+    """Test hook: the next forward's routed gate/up kernel times out (bounded, no hang)."""
+    return load_library().lmoe_debug_inject_wait_timeout(c_vp(ctx))
 
 
 def lmoe_set_cutoff_momentum(ctx, momentum: float) -> int:

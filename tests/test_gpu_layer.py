@@ -254,3 +254,24 @@ def test_streaming_cutoff_matches_oracle():
     with pytest.raises(LmoeError):
         layer.set_cutoff_momentum(1.0)
     layer.close()
+
+
+def test_injected_wait_timeout_is_reported_and_context_recovers():
+    """Failure detection without a GPU fault: the test hook leaves the routed gate/up
+    kernel's token stages unfilled, so its bounded device-side waits (20 ms) run out; the
+    kernel returns, lmoe_sync_status reports LMOE_ERR_TIMEOUT, and the next forward on the
+    same context is bit-identical to one before the failure."""
+    x, weights, bias = make_inputs(WORKLOADS["small_bf16"], "cuda", 300)
+    layer = LatentMoE(SMALL, weights, max_bt=300, router_bias=bias)
+    good = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.sync_status() == L.LMOE_OK
+    assert L.lmoe_debug_inject_wait_timeout(layer.ctx) == L.LMOE_OK
+    layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.sync_status() == L.LMOE_ERR_TIMEOUT
+    again = layer.forward(x)
+    torch.cuda.synchronize()
+    assert layer.sync_status() == L.LMOE_OK
+    assert torch.equal(again, good)
+    layer.close()
