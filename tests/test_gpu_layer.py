@@ -275,3 +275,34 @@ def test_injected_wait_timeout_is_reported_and_context_recovers():
     assert layer.sync_status() == L.LMOE_OK
     assert torch.equal(again, good)
     layer.close()
+
+
+def test_forward_replays_in_a_cuda_graph():
+    """lmoe_forward only encodes tensor maps on the host and launches kernels (no
+    allocation, no synchronisation), so it can be captured in a CUDA graph: replays with new
+    contents in the captured input buffer give the same bits as eager calls."""
+    wl = WORKLOADS["small_bf16"]
+    x0, weights, bias = make_inputs(wl, "cuda", 256)
+    x1 = make_x(wl, "cuda", 256, seed_offset=9)
+    layer = LatentMoE(SMALL, weights, max_bt=256, router_bias=bias)
+    eager0 = layer.forward(x0)
+    eager1 = layer.forward(x1)
+    torch.cuda.synchronize()
+    xin = x0.clone()
+    out = torch.empty_like(eager0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(xin, out, stream=s)      # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(xin, out, stream=s)
+    for xb, want in ((x1, eager1), (x0, eager0), (x1, eager1)):
+        xin.copy_(xb)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
+    assert layer.sync_status() == 0
+    layer.close()
