@@ -31,7 +31,9 @@ Readings of the silent points (the same list is kept with the design notes):
   A6  exactly K experts per token: the K largest keys s - alpha; no capacity, no drops.
   A7  ties go to the lower expert index; idx is ordered by key, descending.
   A8  combine weight w = s / (sum of s over the chosen K); raw scores, not s - alpha.
-  A9  RMSNorm is applied to each (token, expert) latent output, before the weighted sum.
+  A9  RMSNorm is applied to each (token, expert) latent output, before the weighted sum
+      (default).  The other reading, one RMSNorm of the weighted sum in front of W_up, is
+      the option norm="combined".
   A10 eps = 1e-6, learnable gain gamma in R^latent.
   A11 W_up is applied once, to the weighted latent sum.
   A12 layer output = routed + shared (the block residual is outside the layer).
@@ -222,12 +224,26 @@ def _f64(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float64)
 
 
+NORM_PLACEMENTS = ("expert", "combined")
+
+
+def _check_norm(norm: str) -> None:
+    if norm not in NORM_PLACEMENTS:
+        raise ValueError(f"norm must be one of {NORM_PLACEMENTS}, got {norm!r}")
+
+
 def routed_latent(z: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float,
-                  beta_u: float, eps: float) -> np.ndarray:
+                  beta_u: float, eps: float, norm: str = "expert") -> np.ndarray:
     """c[t] = sum_k w[t, k] * RMSNorm(W_d[e] act(W_g[e] z_t, W_u[e] z_t)), e = idx[t, k]:
     the GroupedExperts at latent width followed by latent_norm and the weighted fusion
     ([K3-news] ¶"具体前向流程"; [K3-arch] step e).  Tokens are grouped by expert only so
-    each expert's weights are read once; every (t, k) term is the same matrix-vector work."""
+    each expert's weights are read once; every (t, k) term is the same matrix-vector work.
+
+    norm = "combined" is the other reading of where latent_norm sits ([K3-arch] "Par où
+    l'information passe, pour un seul jeton", step f lists "RMSNorm + W_up" as one step, after
+    the experts): c[t] = RMSNorm(sum_k w[t, k] * W_d[e] act(...)), the weighted sum
+    normalised once."""
+    _check_norm(norm)
     z = _f64(z)
     n, latent = z.shape
     c = np.zeros((n, latent))
@@ -239,9 +255,10 @@ def routed_latent(z: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: 
         wd = _f64(weights["exp_down"][int(e)])
         zr = z[rows]
         a = situ_glu(zr @ wg.T, zr @ wu.T, beta, beta_u)
-        yhat = rms_norm(a @ wd.T, gamma, eps)
-        c[rows] += _f64(w)[rows, ks][:, None] * yhat
-    return c
+        y = a @ wd.T
+        term = rms_norm(y, gamma, eps) if norm == "expert" else y
+        c[rows] += _f64(w)[rows, ks][:, None] * term
+    return rms_norm(c, gamma, eps) if norm == "combined" else c
 
 
 def shared_experts(x: np.ndarray, weights, beta: float, beta_u: float) -> np.ndarray:
@@ -318,10 +335,11 @@ def bf16_round(v) -> np.ndarray:
 
 
 def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weights_fp8, gamma, beta: float,
-                      beta_u: float, eps: float) -> np.ndarray:
+                      beta_u: float, eps: float, norm: str = "expert") -> np.ndarray:
     """routed_latent with fp8 experts: z (the bf16 values the layer stores) quantized per
     token, expert weights given as (q, s) pairs per expert, h quantized with the fixed
-    scale, everything else in fp64."""
+    scale, everything else in fp64.  `norm` places latent_norm as in routed_latent."""
+    _check_norm(norm)
     z = np.asarray(z_bf16, np.float64)
     n, latent = z.shape
     zq, zs = quantize_rows_e4m3(z)
@@ -338,13 +356,15 @@ def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weight
         zr = zd[rows]
         a = situ_glu(zr @ wg.T, zr @ wu.T, beta, beta_u)
         hq = round_e4m3(a * np.float64(r)) * np.float64(s_h)
-        yhat = rms_norm(hq @ wd.T, gamma, eps)
-        c[rows] += _f64(w)[rows, ks][:, None] * yhat
-    return c
+        y = hq @ wd.T
+        term = rms_norm(y, gamma, eps) if norm == "expert" else y
+        c[rows] += _f64(w)[rows, ks][:, None] * term
+    return rms_norm(c, gamma, eps) if norm == "combined" else c
 
 
 def layer_forward_fp8(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, weights_fp8, beta: float = 4.0,
-                      beta_u: float = 25.0, eps: float = 1e-6, z_bf16: np.ndarray | None = None) -> np.ndarray:
+                      beta_u: float = 25.0, eps: float = 1e-6, z_bf16: np.ndarray | None = None,
+                      norm: str = "expert") -> np.ndarray:
     """Layer output with fp8 routed experts (see the fp8 reading above): z = x W_down^T is
     rounded to bf16 as the layer stores it, the routed latent uses routed_latent_fp8, and the
     up projection and shared experts are as in layer_forward.  weights_fp8[e] holds the
@@ -353,12 +373,12 @@ def layer_forward_fp8(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, we
     the same stored values on both sides, as routing takes the same logits)."""
     x = _f64(x)
     z = bf16_round((x @ _f64(weights["w_down"]).T).astype(np.float32)) if z_bf16 is None else _f64(z_bf16)
-    c = routed_latent_fp8(z, idx, w, weights_fp8, weights["latent_gamma"], beta, beta_u, eps)
+    c = routed_latent_fp8(z, idx, w, weights_fp8, weights["latent_gamma"], beta, beta_u, eps, norm)
     return c @ _f64(weights["w_up"]).T + shared_experts(x, weights, beta, beta_u)
 
 
 def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float = 4.0,
-                  beta_u: float = 25.0, eps: float = 1e-6, return_parts: bool = False):
+                  beta_u: float = 25.0, eps: float = 1e-6, return_parts: bool = False, norm: str = "expert"):
     """Stable LatentMoE layer output for the rows of x, given their routing (idx, w).
 
     out = W_up c + shared(x),  c = routed_latent(W_down x)  ([K3-news] ¶"具体前向流程":
@@ -367,10 +387,11 @@ def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: 
 
     `weights` maps names to arrays (or to lazily indexed per-expert providers for the
     expert tensors): w_down [L, d], exp_gate / exp_up [E, I, L], exp_down [E, L, I],
-    latent_gamma [L], w_up [d, L], sh_gate / sh_up [S, Is, d], sh_down [S, d, Is]."""
+    latent_gamma [L], w_up [d, L], sh_gate / sh_up [S, Is, d], sh_down [S, d, Is].
+    `norm` places latent_norm (see routed_latent)."""
     x = _f64(x)
     z = x @ _f64(weights["w_down"]).T
-    c = routed_latent(z, idx, w, weights, beta, beta_u, eps)
+    c = routed_latent(z, idx, w, weights, beta, beta_u, eps, norm)
     routed = c @ _f64(weights["w_up"]).T
     shared = shared_experts(x, weights, beta, beta_u)
     out = routed + shared
@@ -380,11 +401,11 @@ def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: 
 
 
 def forward(x: np.ndarray, weights, top_k: int, router_bias=None, logits=None, beta: float = 4.0,
-            beta_u: float = 25.0, eps: float = 1e-6) -> tuple[np.ndarray, dict]:
+            beta_u: float = 25.0, eps: float = 1e-6, norm: str = "expert") -> tuple[np.ndarray, dict]:
     """Whole layer: route on `logits` if given (e.g. another implementation's fp32 logits,
     upcast exactly), else on this oracle's own fp64 logits; then layer_forward."""
     if logits is None:
         logits = router_logits(x, weights["w_router"], router_bias)
     r = route(logits, top_k)
-    out = layer_forward(x, r["idx"], r["w"], weights, beta, beta_u, eps)
+    out = layer_forward(x, r["idx"], r["w"], weights, beta, beta_u, eps, norm=norm)
     return out, r

@@ -126,3 +126,26 @@ def test_e4m3_round_half_away_is_caught(monkeypatch):
         return np.where(a > 0, np.copysign(q, v), 0.0 * v)
     monkeypatch.setattr(O, "round_e4m3", half_away)
     assert _fails(P.test_round_e4m3_matches_torch_float8)
+
+
+def test_combined_norm_applied_per_expert_is_caught(monkeypatch):
+    orig = O.routed_latent
+    monkeypatch.setattr(O, "routed_latent", lambda z, idx, w, weights, beta, beta_u, eps, norm="expert":
+                        orig(z, idx, w, weights, beta, beta_u, eps, "expert"))
+    assert _fails(P.test_forward_combined_norm_matches_brute_force)
+    assert _fails(P.test_norm_placements_unit_rms_and_single_expert)
+
+
+def test_combined_norm_without_gain_is_caught(monkeypatch):
+    orig = O.rms_norm
+    monkeypatch.setattr(O, "rms_norm", lambda y, gamma, eps=1e-6:
+                        orig(y, np.ones_like(np.asarray(gamma, np.float64)), eps))
+    assert _fails(P.test_combined_norm_torch_library_formulation)
+    assert _fails(P.test_forward_combined_norm_matches_brute_force)
+
+
+
+def test_dropped_latent_norm_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "rms_norm", lambda y, gamma, eps=1e-6: np.asarray(y, np.float64))
+    assert _fails(P.test_norm_placements_unit_rms_and_single_expert)
+    assert _fails(P.test_forward_combined_norm_matches_brute_force)

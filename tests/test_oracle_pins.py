@@ -261,8 +261,9 @@ def _tiny(seed=0, **kw):
     return shape, _np(x), _weights_np(weights), (None if bias is None else _np(bias))
 
 
-def _brute_forward(x, weights, shape, logits):
-    """Per-token loops over explicit dot products; no grouping, no vectorised routing."""
+def _brute_forward(x, weights, shape, logits, norm="expert"):
+    """Per-token loops over explicit dot products; no grouping, no vectorised routing.
+    norm="combined" normalises the weighted latent sum instead of each expert's output."""
     bt, E, K = x.shape[0], shape.n_experts, shape.top_k
     s = [[1 / (1 + math.exp(-logits[t][e])) for e in range(E)] for t in range(bt)]
     j = ((bt - 1) * (E - K)) // E
@@ -292,9 +293,13 @@ def _brute_forward(x, weights, shape, logits):
             u = matvec(weights["exp_up"][e], z)
             a = [act(g[i], u[i]) for i in range(len(g))]
             y = matvec(weights["exp_down"][e], a)
-            rms = math.sqrt(sum(v * v for v in y) / len(y) + shape.rms_eps)
+            rms = math.sqrt(sum(v * v for v in y) / len(y) + shape.rms_eps) if norm == "expert" else 1.0
             for i in range(len(y)):
-                c[i] += s[t][e] / tot * weights["latent_gamma"][i] * y[i] / rms
+                gain = weights["latent_gamma"][i] if norm == "expert" else 1.0
+                c[i] += s[t][e] / tot * gain * y[i] / rms
+        if norm == "combined":
+            rms = math.sqrt(sum(v * v for v in c) / len(c) + shape.rms_eps)
+            c = [weights["latent_gamma"][i] * c[i] / rms for i in range(len(c))]
         o = matvec(weights["w_up"], c)
         for jsh in range(shape.n_shared):
             g = matvec(weights["sh_gate"][jsh], x[t])
@@ -311,6 +316,57 @@ def test_forward_matches_brute_force():
     out, r = O.forward(x, W, shape.top_k, logits=logits)
     ref = _brute_forward(x, W, shape, logits)
     np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_forward_combined_norm_matches_brute_force():
+    """The other placement of latent_norm (one RMSNorm of the weighted sum, in front of
+    W_up) against the per-token loops with the norm moved after the sum."""
+    shape, x, W, _ = _tiny(seed=2, gamma_noise=0.1)
+    logits = O.router_logits(x, W["w_router"]) * 40.0
+    out, _ = O.forward(x, W, shape.top_k, logits=logits, norm="combined")
+    ref = _brute_forward(x, W, shape, logits, norm="combined")
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-12)
+    # and it is a different layer from the per-expert placement
+    per_expert = _brute_forward(x, W, shape, logits)
+    assert np.abs(out - per_expert).max() > 1e-3
+
+
+def test_combined_norm_torch_library_formulation():
+    """c = rms_norm(sum_k w_k y_k) written with torch fp64 routines, on the oracle's routing."""
+    shape, x, W, _ = _tiny(seed=6, gamma_noise=0.1)
+    r = O.route(O.router_logits(x, W["w_router"]) * 40, shape.top_k)
+    TW = {k: torch.from_numpy(v) for k, v in W.items()}
+    z = F.linear(torch.from_numpy(x), TW["w_down"])
+    craw = torch.zeros(x.shape[0], shape.latent, dtype=torch.float64)
+    for t in range(x.shape[0]):
+        for k in range(shape.top_k):
+            e = int(r["idx"][t, k])
+            g = 4.0 * torch.tanh(F.linear(z[t], TW["exp_gate"][e]) / 4.0)
+            a = F.silu(g) * 25.0 * torch.tanh(F.linear(z[t], TW["exp_up"][e]) / 25.0)
+            craw[t] += float(r["w"][t, k]) * F.linear(a, TW["exp_down"][e])
+    ref = F.rms_norm(craw, (shape.latent,), TW["latent_gamma"], eps=1e-6).numpy()
+    got = O.routed_latent(z.numpy(), r["idx"], r["w"], W, 4.0, 25.0, 1e-6, norm="combined")
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_norm_placements_unit_rms_and_single_expert():
+    """With gamma = 1 and eps = 0 the combined placement gives every c row RMS exactly 1;
+    the per-expert placement gives a convex mix of unit-RMS rows, so RMS <= 1 (strictly
+    below for K > 1 unless the rows align).  With K = 1 (w = 1) the placements coincide."""
+    shape, x, W, _ = _tiny(seed=4)
+    W = dict(W, latent_gamma=np.ones(shape.latent))
+    r = O.route(O.router_logits(x, W["w_router"]) * 40, shape.top_k)
+    z = x @ W["w_down"].T
+    cc = O.routed_latent(z, r["idx"], r["w"], W, 4.0, 25.0, 0.0, norm="combined")
+    ce = O.routed_latent(z, r["idx"], r["w"], W, 4.0, 25.0, 0.0, norm="expert")
+    np.testing.assert_allclose(np.sqrt((cc ** 2).mean(1)), 1.0, rtol=1e-12)
+    assert np.all(np.sqrt((ce ** 2).mean(1)) < 1.0 - 1e-6)
+    r1 = O.route(O.router_logits(x, W["w_router"]) * 40, 1)
+    c1 = O.routed_latent(z, r1["idx"], r1["w"], W, 4.0, 25.0, 1e-6, norm="combined")
+    e1 = O.routed_latent(z, r1["idx"], r1["w"], W, 4.0, 25.0, 1e-6, norm="expert")
+    np.testing.assert_allclose(c1, e1, rtol=1e-12, atol=1e-14)
+    with pytest.raises(ValueError):
+        O.routed_latent(z, r["idx"], r["w"], W, 4.0, 25.0, 1e-6, norm="latent")
 
 
 def test_forward_torch_library_formulation():
