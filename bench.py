@@ -371,6 +371,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--fp8-experts", action="store_true",
                     help="routed experts in e4m3 (lmoe_create_fp8); a separate line, not the bf16 headline")
+    ap.add_argument("--latent-norm", default="expert", choices=["expert", "combined"],
+                    help="latent RMSNorm placement; 'combined' (one norm of the weighted sum) is a separate line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -400,6 +402,8 @@ def main(argv=None):
         layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias, fp8_experts=f8)
     else:
         layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias)
+    if args.latent_norm != "expert":
+        layer.set_latent_norm(args.latent_norm)
     out = torch.empty((w.bt, s.d), dtype=layer.dtype, device=device)
     stream = torch.cuda.current_stream(device)
 
@@ -486,7 +490,7 @@ def main(argv=None):
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.fp8_experts:
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.fp8_experts and args.latent_norm == "expert":
         t = oracle_sample_time(w, x, weights, bias, args.cpu_tokens)
         cpu = {"value": args.cpu_tokens / t, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{args.cpu_tokens} tokens spread over the batch, routed among themselves, "
@@ -511,6 +515,9 @@ def main(argv=None):
         if args.fp8_experts:
             line["dtype"] = "bf16 (routed experts e4m3)"
             line["metric"] = METRIC + " [fp8 routed experts]"
+        if args.latent_norm != "expert":
+            line["metric"] += f" [latent norm: {args.latent_norm}]"
+            line["config"]["latent_norm"] = args.latent_norm
         print(json.dumps(line), flush=True)
     layer.close()
     if ws > 1:

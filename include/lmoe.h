@@ -178,6 +178,20 @@ LMOE_API lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* ou
  * context or m outside [0, 1); no GPU work. */
 LMOE_API lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum);
 
+/* Placement of the latent RMSNorm.  LMOE_NORM_PER_EXPERT (the default) normalises each
+ * (token, expert) latent output before the weighted fusion ("KimiK3的StableLatentMoE架构解析",
+ * ¶"具体前向流程" and ¶"第二"):  c = sum_k w_k * gamma * y_k / rms(y_k).
+ * LMOE_NORM_COMBINED normalises the weighted sum once, in front of W_up ("Vue d'ensemble de
+ * l'architecture", "Par où l'information passe, pour un seul jeton", step f "RMSNorm + W_up"):
+ *     c = gamma * s / rms(s),  s = sum_k w_k * y_k,  rms(v) = sqrt(mean(v^2) + rms_eps).
+ * Applies to every later lmoe_forward on this context (bf16, fp32 and fp8-expert layers).
+ * Returns LMOE_ERR_INVALID_ARG for a NULL context or an unknown placement,
+ * LMOE_ERR_UNSUPPORTED for LMOE_NORM_COMBINED with latent > 49152, LMOE_ERR_CUDA if the
+ * combine kernel's shared memory limit cannot be raised on the current device.  No GPU
+ * work is enqueued. */
+typedef enum { LMOE_NORM_PER_EXPERT = 0, LMOE_NORM_COMBINED = 1 } lmoe_latent_norm;
+LMOE_API lmoe_status lmoe_set_latent_norm(lmoe_ctx* ctx, lmoe_latent_norm placement);
+
 /* Failure-detection test hook.  Arms the next lmoe_forward on this context so that its
  * routed-expert gate/up kernel leaves its token stages unfilled and limits its device-side
  * waits to 20 ms: the waits run out, the kernel records the timeout in the status word,

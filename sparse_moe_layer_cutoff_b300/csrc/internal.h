@@ -91,7 +91,12 @@ struct CombineArgs {
   int bt, top_k, latent;
   float eps;
   void* cat; long long ldc;   // c written to cat[t, 0:L]
+  bool norm_sum;              // RMSNorm of the weighted sum instead of each expert row
 };
+// Largest latent width the norm-on-sum combine supports (its fp32 row lives in shared memory).
+constexpr int kMaxNormSumLatent = 48 * 1024;
+// Raises the combine kernel's dynamic shared memory limit for norm_sum at this latent width.
+cudaError_t prepare_combine(int latent, bool norm_sum);
 cudaError_t launch_combine(const CombineArgs& a, bool is_bf16, cudaStream_t st);
 
 }  // namespace lmoe

@@ -29,6 +29,7 @@ struct lmoe_ctx {
   int last_bt;
   double momentum;      // streaming cutoffs: weight of the previous call's cutoff (0 = per call)
   bool state_valid;     // a call has stored its cutoff since momentum was set
+  bool norm_sum;        // latent RMSNorm on the weighted sum instead of each expert row
   // workspace (one allocation)
   char* ws;
   size_t ws_bytes;
@@ -431,6 +432,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     a.y = ctx->y; a.inv = ctx->inv; a.w = ctx->wk; a.gamma = ctx->w.latent_gamma;
     a.bt = bt; a.top_k = c.top_k; a.latent = c.latent; a.eps = c.rms_eps;
     a.cat = ctx->cat; a.ldc = ldc;
+    a.norm_sum = ctx->norm_sum;
     e = launch_combine(a, ctx->bf16, st);
     ctx->launches += 1;
     prof_mark(ctx, 6, st);
@@ -473,6 +475,18 @@ lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum) {
   if (!ctx || !(momentum >= 0.0 && momentum < 1.0)) return LMOE_ERR_INVALID_ARG;
   ctx->momentum = momentum;
   ctx->state_valid = false;
+  return LMOE_OK;
+}
+
+lmoe_status lmoe_set_latent_norm(lmoe_ctx* ctx, lmoe_latent_norm placement) {
+  if (!ctx || (placement != LMOE_NORM_PER_EXPERT && placement != LMOE_NORM_COMBINED)) return LMOE_ERR_INVALID_ARG;
+  const bool norm_sum = placement == LMOE_NORM_COMBINED;
+  if (norm_sum && ctx->cfg.latent > kMaxNormSumLatent) return LMOE_ERR_UNSUPPORTED;
+  if (prepare_combine(ctx->cfg.latent, norm_sum) != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
+  }
+  ctx->norm_sum = norm_sum;
   return LMOE_OK;
 }
 

@@ -97,6 +97,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_debug_inject_wait_timeout.restype = c_i32
     lib.lmoe_set_cutoff_momentum.argtypes = [c_vp, ctypes.c_double]
     lib.lmoe_set_cutoff_momentum.restype = c_i32
+    lib.lmoe_set_latent_norm.argtypes = [c_vp, c_i32]
+    lib.lmoe_set_latent_norm.restype = c_i32
     lib.lmoe_profile.argtypes = [c_vp, c_i32]
     lib.lmoe_profile.restype = c_i32
     lib.lmoe_profile_read.argtypes = [c_vp, ctypes.POINTER(c_f32), ctypes.POINTER(c_i32),
@@ -228,6 +230,15 @@ def lmoe_set_cutoff_momentum(ctx, momentum: float) -> int:
     return load_library().lmoe_set_cutoff_momentum(c_vp(ctx), float(momentum))
 
 
+LMOE_NORM_PER_EXPERT, LMOE_NORM_COMBINED = 0, 1
+NORM_PLACEMENTS = {"expert": LMOE_NORM_PER_EXPERT, "combined": LMOE_NORM_COMBINED}
+
+
+def lmoe_set_latent_norm(ctx, placement: int) -> int:
+    """Latent RMSNorm on each expert output (0) or once on their weighted sum (1)."""
+    return load_library().lmoe_set_latent_norm(c_vp(ctx), int(placement))
+
+
 def lmoe_profile(ctx, enable: bool) -> int:
     return load_library().lmoe_profile(c_vp(ctx), 1 if enable else 0)
 
@@ -337,6 +348,15 @@ class LatentMoE:
         st = lmoe_set_cutoff_momentum(self.ctx, momentum)
         if st != LMOE_OK:
             raise LmoeError(st, "lmoe_set_cutoff_momentum")
+
+    def set_latent_norm(self, placement: str) -> None:
+        """"expert" (default): RMSNorm of each expert's latent output before the weighted sum;
+        "combined": one RMSNorm of the weighted sum, in front of W_up."""
+        if placement not in NORM_PLACEMENTS:
+            raise ValueError(f"placement must be one of {tuple(NORM_PLACEMENTS)}, got {placement!r}")
+        st = lmoe_set_latent_norm(self.ctx, NORM_PLACEMENTS[placement])
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_set_latent_norm")
 
     def workspace(self) -> lmoe_workspace_view:
         return lmoe_workspace(self.ctx)

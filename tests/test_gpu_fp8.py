@@ -9,7 +9,7 @@ from oracle import lmoe_oracle as O
 from sparse_moe_layer_cutoff_b300 import LatentMoE, LmoeError
 from sparse_moe_layer_cutoff_b300 import lmoe as L
 from sparse_moe_layer_cutoff_b300.lmoe import workspace_tensors
-from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, oracle_weights, rel_l2, to64
+from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, latent_norm_scale, oracle_weights, rel_l2, to64
 from workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -67,12 +67,14 @@ class Fp8Experts:
         return tuple(out)
 
 
-def _run_fp8(wl, bt, rows=None):
+def _run_fp8(wl, bt, rows=None, norm="expert"):
     x, weights, bias = make_inputs(wl, "cuda", bt)
     f8 = L.quantize_experts_fp8(weights)
     s = wl.shape
     dense = {k: v for k, v in weights.items() if not k.startswith("exp_")}
     layer = LatentMoE(s, dense, max_bt=bt, router_bias=bias, fp8_experts=f8)
+    if norm != "expert":
+        layer.set_latent_norm(norm)
     r = layer.route(x)
     out = layer.forward(x)
     torch.cuda.synchronize()
@@ -85,17 +87,18 @@ def _run_fp8(wl, bt, rows=None):
     # enter its router: both sides then take the same discrete quantization decisions
     z = to64(workspace_tensors(layer)["z"][torch.as_tensor(rows, device="cuda")])
     want = O.layer_forward_fp8(to64(x[rows]), ref["idx"][rows], ref["w"][rows], oracle_weights(weights),
-                               Fp8Experts(f8), s.beta, s.beta_u, s.rms_eps, z_bf16=z)
+                               Fp8Experts(f8), s.beta, s.beta_u, s.rms_eps, z_bf16=z, norm=norm)
     # and the stored z itself is the bf16 rounding of x W_down^T, to a few bf16 steps
     z_ref = to64(x[rows]) @ to64(weights["w_down"]).T
     assert rel_l2(z, z_ref) < 4e-3
     got = to64(out[rows])
     m = float(np.abs(got - want).max())
     rl = rel_l2(got, want)
-    assert m <= BF16_MAX_ABS and rl <= BF16_REL_L2, (m, rl)
+    k = latent_norm_scale(z_ref, ref["idx"][rows], ref["w"][rows], oracle_weights(weights), s, norm)
+    assert m <= BF16_MAX_ABS * k and rl <= BF16_REL_L2, (m, rl, k)
     # the fp8 layer stays close to the bf16 one (e4m3 rounding only)
     want16 = O.layer_forward(to64(x[rows]), ref["idx"][rows], ref["w"][rows], oracle_weights(weights), s.beta,
-                             s.beta_u, s.rms_eps)
+                             s.beta_u, s.rms_eps, norm=norm)
     assert rel_l2(got, want16) < 0.1
     layer.close()
 
@@ -103,6 +106,10 @@ def _run_fp8(wl, bt, rows=None):
 @pytest.mark.parametrize("bt", [300, 1, 77])
 def test_fp8_layer_small_matches_oracle(bt):
     _run_fp8(WORKLOADS["small_bf16"], bt)
+
+
+def test_fp8_layer_combined_latent_norm():
+    _run_fp8(WORKLOADS["small_bf16"], 300, norm="combined")
 
 
 def test_fp8_layer_full_decode():

@@ -306,3 +306,53 @@ def test_forward_replays_in_a_cuda_graph():
         assert torch.equal(out, want)
     assert layer.sync_status() == 0
     layer.close()
+
+
+@pytest.mark.parametrize("name,bt", [("tiny_f32", 64), ("small_bf16", 300), ("small_bf16", 2048)])
+def test_combined_latent_norm_matches_oracle(name, bt):
+    """lmoe_set_latent_norm(LMOE_NORM_COMBINED): one RMSNorm of the weighted latent sum.
+    The stored c against the oracle's routed_latent(norm="combined"), then the output."""
+    r = Run(WORKLOADS[name], bt=bt, norm="combined")
+    assert r.status == 0
+    ref = r.check_routing()
+    s = r.shape
+    W = oracle_weights(r.weights)
+    c_ref = O.routed_latent(to64(r.x) @ W["w_down"].T, ref["idx"], ref["w"], W, s.beta, s.beta_u, s.rms_eps,
+                            norm="combined")
+    c = to64(r.ws["cat"])[:, : s.latent]
+    assert rel_l2(c, c_ref) < (1e-5 if s.dtype == "f32" else 2e-2)
+    r.check_output(ref_route=ref)
+    # and it is not the per-expert layer
+    per_expert = O.routed_latent(to64(r.x) @ W["w_down"].T, ref["idx"], ref["w"], W, s.beta, s.beta_u,
+                                 s.rms_eps)
+    assert rel_l2(c, per_expert) > 0.1
+    r.close()
+
+
+def test_combined_latent_norm_full_decode_sampled_rows():
+    w = WORKLOADS["full_decode_bt64"]
+    r = Run(w, norm="combined")
+    assert r.status == 0
+    r.check_output(rows=_sample_rows(r.bt))
+    r.close()
+
+
+def test_latent_norm_switch_and_argument_errors():
+    """Switching the placement back gives the per-expert layer's bits again; unknown
+    placements are refused on the host."""
+    wl = WORKLOADS["small_bf16"]
+    x, weights, bias = make_inputs(wl, "cuda", 200)
+    layer = LatentMoE(SMALL, weights, max_bt=200, router_bias=bias)
+    a = layer.forward(x).clone()
+    layer.set_latent_norm("combined")
+    b = layer.forward(x).clone()
+    layer.set_latent_norm("expert")
+    c = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, c) and not torch.equal(a, b)
+    assert L.lmoe_set_latent_norm(layer.ctx, 2) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_set_latent_norm(None, L.LMOE_NORM_COMBINED) == L.LMOE_ERR_INVALID_ARG
+    with pytest.raises(ValueError):
+        layer.set_latent_norm("latent")
+    assert layer.sync_status() == 0
+    layer.close()
