@@ -136,6 +136,21 @@ LMOE_API lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void
  * LMOE_OK, LMOE_ERR_TIMEOUT or LMOE_ERR_DEVICE_ASSERT. */
 LMOE_API lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream);
 
+/* lmoe_forward with the input and output in host memory: x_host [bt, d] and out_host [bt, d],
+ * both of cfg.dtype, page-locked (cudaHostAlloc / cudaHostRegister) for copies that overlap
+ * the GPU's work, or pageable (then each copy also stalls the calling thread).  The context
+ * stages them through device buffers it owns (3 x max_bt x d elements, allocated by the first
+ * call, which therefore synchronises the device and cannot be captured in a CUDA graph).
+ * The input copy runs on an internal copy stream into one of two staging buffers, so it
+ * overlaps the previous call's forward; it reads x_host at some point after the call is made,
+ * so x_host must already hold the input when lmoe_forward_host is called and stay unchanged
+ * until `stream` passes the call.  The forward and the output copy run on `stream`: out_host
+ * is written when `stream` passes the call.  Errors: as lmoe_forward; LMOE_ERR_INVALID_ARG
+ * also for device or managed pointers and overlapping x_host / out_host; LMOE_ERR_OOM if the
+ * staging buffers cannot be allocated. */
+LMOE_API lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host,
+                                       lmoe_stream stream);
+
 /* Synchronise the context's work, free its workspace and the context.  NULL is a no-op. */
 LMOE_API void lmoe_destroy(lmoe_ctx* ctx);
 

@@ -59,6 +59,12 @@ struct lmoe_ctx {
   std::vector<cudaEvent_t> prof_ev;   // [kProfCap][LMOE_NUM_STAGES + 1]
   long long launches;
   long long prof_launch_base;
+  // host-buffer entry point (created by its first call)
+  char* host_ws;             // two x staging buffers, then one out buffer, [max_bt, d] each
+  cudaStream_t host_cs;      // copy stream of the input copies
+  cudaEvent_t host_in[2];    // input copy into staging buffer b done
+  cudaEvent_t host_used[2];  // the forward that read staging buffer b done
+  int host_next;
 };
 
 namespace {
@@ -120,6 +126,20 @@ struct Carve {
     return o;
   }
 };
+
+// Staging buffers, copy stream and events of lmoe_forward_host (no-op if never created).
+void release_host_io(lmoe_ctx* ctx) {
+  for (int b = 0; b < 2; ++b) {
+    if (ctx->host_in[b]) cudaEventDestroy(ctx->host_in[b]);
+    if (ctx->host_used[b]) cudaEventDestroy(ctx->host_used[b]);
+    ctx->host_in[b] = ctx->host_used[b] = nullptr;
+  }
+  if (ctx->host_cs) cudaStreamDestroy(ctx->host_cs);
+  ctx->host_cs = nullptr;
+  cudaFree(ctx->host_ws);
+  ctx->host_ws = nullptr;
+  ctx->host_next = 0;
+}
 
 lmoe_status finish(lmoe_ctx* ctx, cudaStream_t st, cudaError_t e) {
   if (e != cudaSuccess) return LMOE_ERR_CUDA;
@@ -539,9 +559,71 @@ lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream) {
   return LMOE_OK;
 }
 
+lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host, lmoe_stream stream) {
+  if (!ctx || bt < 0 || bt > ctx->max_bt) return LMOE_ERR_INVALID_ARG;
+  if (bt == 0) return LMOE_OK;
+  if (!x_host || !out_host) return LMOE_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)bt * ctx->cfg.d * ctx->esz;
+  const char* xb = static_cast<const char*>(x_host);
+  const char* ob = static_cast<const char*>(out_host);
+  if (ob < xb + bytes && xb < ob + bytes) return LMOE_ERR_INVALID_ARG;  // out overlaps x
+  for (const void* p : {x_host, static_cast<const void*>(out_host)}) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return LMOE_ERR_INVALID_ARG;
+    }
+    if (at.type != cudaMemoryTypeHost && at.type != cudaMemoryTypeUnregistered) return LMOE_ERR_INVALID_ARG;
+  }
+  if (!ctx->host_ws) {  // first call: staging buffers, copy stream, events
+    const size_t one = align_up((size_t)ctx->max_bt * ctx->cfg.d * ctx->esz, 256);
+    if (cudaMalloc(&ctx->host_ws, 3 * one) != cudaSuccess) {
+      cudaGetLastError();
+      ctx->host_ws = nullptr;
+      return LMOE_ERR_OOM;
+    }
+    bool ok = cudaStreamCreateWithFlags(&ctx->host_cs, cudaStreamNonBlocking) == cudaSuccess;
+    for (int b = 0; b < 2 && ok; ++b)
+      ok = cudaEventCreateWithFlags(&ctx->host_in[b], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&ctx->host_used[b], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) {
+      cudaGetLastError();
+      release_host_io(ctx);
+      return LMOE_ERR_CUDA;
+    }
+  }
+  const size_t one = align_up((size_t)ctx->max_bt * ctx->cfg.d * ctx->esz, 256);
+  const int b = ctx->host_next;
+  char* xd = ctx->host_ws + (size_t)b * one;
+  char* od = ctx->host_ws + 2 * one;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // input copy on the copy stream, once the forward that last read this staging buffer is done;
+  // it overlaps whatever runs on the caller's stream before this call (the previous forward)
+  cudaError_t e = cudaStreamWaitEvent(ctx->host_cs, ctx->host_used[b], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, ctx->host_cs);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->host_in[b], ctx->host_cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->host_in[b], 0);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
+  }
+  ctx->host_next = b ^ 1;
+  const lmoe_status s = lmoe_forward(ctx, xd, bt, od, stream);
+  if (s != LMOE_OK) return s;
+  e = cudaEventRecord(ctx->host_used[b], st);
+  // output copy in stream order: done when the caller's stream passes this call
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
+  }
+  return LMOE_OK;
+}
+
 void lmoe_destroy(lmoe_ctx* ctx) {
   if (!ctx) return;
   cudaDeviceSynchronize();
+  release_host_io(ctx);
   for (auto& ev : ctx->prof_ev) cudaEventDestroy(ev);
   tc_plan_destroy(ctx->tc);
   cudaFree(ctx->ws);

@@ -72,6 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_route.restype = c_i32
     lib.lmoe_forward.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
     lib.lmoe_forward.restype = c_i32
+    lib.lmoe_forward_host.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
+    lib.lmoe_forward_host.restype = c_i32
     lib.lmoe_sync_status.argtypes = [c_vp, c_vp]
     lib.lmoe_sync_status.restype = c_i32
     lib.lmoe_destroy.argtypes = [c_vp]
@@ -141,6 +143,11 @@ def lmoe_route(ctx, x: int, bt: int, stream: int = 0, topk_idx: int = 0, topk_w:
 
 def lmoe_forward(ctx, x: int, bt: int, out: int, stream: int = 0) -> int:
     return load_library().lmoe_forward(c_vp(ctx), c_vp(x), bt, c_vp(out), c_vp(stream))
+
+
+def lmoe_forward_host(ctx, x_host: int, bt: int, out_host: int, stream: int = 0) -> int:
+    """lmoe_forward with x and out in host memory (staged by the context)."""
+    return load_library().lmoe_forward_host(c_vp(ctx), c_vp(x_host), bt, c_vp(out_host), c_vp(stream))
 
 
 def lmoe_sync_status(ctx, stream: int = 0) -> int:
@@ -338,6 +345,19 @@ class LatentMoE:
         st = lmoe_forward(self.ctx, x.data_ptr(), x.shape[0], out.data_ptr(), self._stream(stream))
         if st != LMOE_OK:
             raise LmoeError(st, "lmoe_forward")
+        return out
+
+    def forward_host(self, x, out=None, stream=None):
+        """Forward of a CPU tensor x (pinned for overlapped copies) into a CPU tensor out; out is
+        ready once `stream` (default: the current one) passes the call."""
+        import torch
+        if x.device.type != "cpu":
+            raise ValueError("forward_host takes a CPU tensor; use forward for device tensors")
+        if out is None:
+            out = torch.empty((x.shape[0], self.shape.d), dtype=self.dtype, pin_memory=x.is_pinned())
+        st = lmoe_forward_host(self.ctx, x.data_ptr(), x.shape[0], out.data_ptr(), self._stream(stream))
+        if st != LMOE_OK:
+            raise LmoeError(st, "lmoe_forward_host")
         return out
 
     def sync_status(self, stream=None) -> int:

@@ -356,3 +356,50 @@ def test_latent_norm_switch_and_argument_errors():
         layer.set_latent_norm("latent")
     assert layer.sync_status() == 0
     layer.close()
+
+
+@pytest.mark.parametrize("name", ["small_bf16", "tiny_f32"])
+def test_forward_host_matches_device_forward(name):
+    """lmoe_forward_host (host input and output, staged by the context through two input
+    buffers and a copy stream): back-to-back calls with no synchronisation in between give the
+    bits of device-buffer forwards of the same inputs; pageable buffers work too."""
+    wl = WORKLOADS[name]
+    bt = 300 if name == "small_bf16" else 64
+    x0, weights, bias = make_inputs(wl, "cuda", bt)
+    xs = [x0] + [make_x(wl, "cuda", bt, seed_offset=k) for k in (3, 4, 5)]
+    layer = LatentMoE(wl.shape, weights, max_bt=512, router_bias=bias)
+    want = [layer.forward(x).cpu() for x in xs]
+    torch.cuda.synchronize()
+    hx = [x.cpu().pin_memory() for x in xs]
+    outs = [torch.empty_like(w).pin_memory() for w in want * 2]
+    for i, o in enumerate(outs):          # 8 calls queued, inputs reused in rotation
+        layer.forward_host(hx[i % 4], o)
+    torch.cuda.synchronize()
+    for i, o in enumerate(outs):
+        assert torch.equal(o, want[i % 4]), i
+    # pageable host memory, and a ragged batch below the first one's size
+    got = layer.forward_host(xs[1].cpu()[:77].clone())
+    torch.cuda.synchronize()
+    assert torch.equal(got, layer.forward(xs[1][:77]).cpu())
+    assert layer.sync_status() == 0
+    layer.close()
+
+
+def test_forward_host_argument_errors():
+    wl = WORKLOADS["small_bf16"]
+    x, weights, bias = make_inputs(wl, "cuda", 8)
+    layer = LatentMoE(SMALL, weights, max_bt=8, router_bias=bias)
+    xh = x.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    od = torch.empty_like(x)
+    ctx = layer.ctx
+    assert L.lmoe_forward_host(ctx, x.data_ptr(), 8, oh.data_ptr()) == L.LMOE_ERR_INVALID_ARG   # device input
+    assert L.lmoe_forward_host(ctx, xh.data_ptr(), 8, od.data_ptr()) == L.LMOE_ERR_INVALID_ARG  # device output
+    assert L.lmoe_forward_host(ctx, xh.data_ptr(), 9, oh.data_ptr()) == L.LMOE_ERR_INVALID_ARG  # bt > max_bt
+    assert L.lmoe_forward_host(ctx, xh.data_ptr(), 8, xh.data_ptr()) == L.LMOE_ERR_INVALID_ARG  # out overlaps x
+    assert L.lmoe_forward_host(ctx, 0, 8, oh.data_ptr()) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_forward_host(ctx, 0, 0, 0) == L.LMOE_OK
+    with pytest.raises(ValueError):
+        layer.forward_host(x)
+    assert layer.sync_status() == 0
+    layer.close()
