@@ -408,10 +408,13 @@ def main(argv=None):
     stream = torch.cuda.current_stream(device)
 
     # experts touched (for the algorithmic byte count), from the route of each batch
-    touched = []
+    touched, load_max, load_min = [], [], []
     for xb in xs:
         r = layer.route(xb)
-        touched.append(int((r["counts"] > 0).sum().item()))
+        c = r["counts"]
+        touched.append(int((c > 0).sum().item()))
+        load_max.append(int(c.max().item()))
+        load_min.append(int(c.min().item()))
     n_touched = sum(touched) / len(touched)
 
     for i in range(args.warmup):
@@ -463,7 +466,9 @@ def main(argv=None):
     step_s = ms / 1e3 / args.steps
     layer_roof = {"tflops": flops / step_s / 1e12, "tc_frac": flops / step_s / 1e12 / pk["tc"],
                   "gbs": layer_bytes / step_s / 1e9, "hbm_frac": layer_bytes / step_s / 1e9 / pk["hbm"],
-                  "algorithmic_flops": flops, "algorithmic_bytes": layer_bytes, "experts_touched": n_touched}
+                  "algorithmic_flops": flops, "algorithmic_bytes": layer_bytes, "experts_touched": n_touched,
+                  "expert_load": {"max": max(load_max), "min": min(load_min),
+                                  "target": w.bt * s.top_k / s.n_experts}}
 
     # ---- end to end through the C ABI host-buffer call (lmoe_forward_host): every step copies
     # its input from pinned host memory and its output back to pinned host memory.  Wall clock

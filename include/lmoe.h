@@ -133,7 +133,12 @@ LMOE_API lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_s
 LMOE_API lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream);
 
 /* Synchronise `stream`, then return (and clear) the device status word of the context:
- * LMOE_OK, LMOE_ERR_TIMEOUT or LMOE_ERR_DEVICE_ASSERT. */
+ * LMOE_OK, LMOE_ERR_TIMEOUT or LMOE_ERR_DEVICE_ASSERT.
+ * Environment: LMOE_CHECK=1 at lmoe_create makes every call of the context synchronise and
+ * return this status, and validates the routing index buffers before they are used (see
+ * lmoe_debug_check_segments); LMOE_LOG=1 prints one line on stderr for every failing call of
+ * this API.  Each lmoe_forward is annotated with NVTX ranges ("lmoe_forward" and one per
+ * stage, named as the stages of lmoe_profile) for profilers. */
 LMOE_API lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream);
 
 /* lmoe_forward with the input and output in host memory: x_host [bt, d] and out_host [bt, d],
@@ -215,6 +220,21 @@ LMOE_API lmoe_status lmoe_set_latent_norm(lmoe_ctx* ctx, lmoe_latent_norm placem
  * LMOE_ERR_TIMEOUT (and clears it) and later calls work normally.  LMOE_ERR_UNSUPPORTED on the
  * CUDA-core engine (fp32 layers). */
 LMOE_API lmoe_status lmoe_debug_inject_wait_timeout(lmoe_ctx* ctx);
+
+/* Check of the routing index buffers (the same check LMOE_CHECK=1 runs inside every
+ * lmoe_route / lmoe_forward before any kernel indexes memory through them): on the last bt
+ * tokens routed on this context, every expert id is in [0, n_experts) and a token's K ids are
+ * distinct, the offsets start at 0 and end at bt*K with counts[e] = offsets[e+1] - offsets[e],
+ * and every (t, k) slot lies in its expert's segment with perm[slot] = t, so the segments are
+ * a permutation of the bt*K (token, k) pairs.  Synchronises `stream`; returns LMOE_OK,
+ * LMOE_ERR_DEVICE_ASSERT if a check failed (the status word is cleared), LMOE_OK if nothing
+ * has been routed yet. */
+LMOE_API lmoe_status lmoe_debug_check_segments(lmoe_ctx* ctx, lmoe_stream stream);
+
+/* Failure-injection test hook on the host: the next device allocation the library makes for a
+ * context workspace (lmoe_create, lmoe_create_fp8) or for lmoe_forward_host's staging buffers
+ * fails, and that call returns LMOE_ERR_OOM with nothing leaked.  Process-wide, one shot. */
+LMOE_API void lmoe_debug_fail_next_alloc(void);
 
 /* Per-stage device timing.  lmoe_profile(ctx, 1) clears the record and starts recording
  * CUDA events on the call's stream at every stage boundary of each lmoe_forward (up to

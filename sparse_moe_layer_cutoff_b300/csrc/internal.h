@@ -82,6 +82,13 @@ cudaError_t launch_gemm_simt(const GemmArgs& a, bool is_bf16, cudaStream_t st);
 cudaError_t launch_gather_quant(const void* z, const int32_t* perm, const int32_t* offsets, int n_experts, int latent,
                                 void* zq, float* tscale, int grid, cudaStream_t st);
 
+// ---------------------------------------------------------------------------- checks
+// Sets kStatusAssert in *status unless idx / counts / offsets / perm / inv form valid
+// expert segments of bt*top_k (token, k) pairs (csrc/check.cu).
+cudaError_t launch_validate_segments(const int32_t* idx, const int32_t* counts, const int32_t* offsets,
+                                     const int32_t* perm, const int32_t* inv, int bt, int top_k, int n_experts,
+                                     uint32_t* status, int sm_count, cudaStream_t st);
+
 // ---------------------------------------------------------------------------- combine
 struct CombineArgs {
   const void* y;          // [bt*K, L] slot-ordered expert outputs

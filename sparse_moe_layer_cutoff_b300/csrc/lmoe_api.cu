@@ -2,6 +2,9 @@
 // launch sequence of the layer ("KimiK3的StableLatentMoE架构解析", ¶"具体前向流程" / Fig. 2:
 // router -> down_proj -> GroupedExperts -> latent_norm + weighted fusion -> up_proj, plus the
 // shared SiTU-GLU branch on the flattened input).
+#include <nvtx3/nvToolsExt.h>
+
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -65,6 +68,7 @@ struct lmoe_ctx {
   cudaEvent_t host_in[2];    // input copy into staging buffer b done
   cudaEvent_t host_used[2];  // the forward that read staging buffer b done
   int host_next;
+  int nvtx_open;             // NVTX ranges this forward has pushed and not yet popped
 };
 
 namespace {
@@ -74,6 +78,54 @@ constexpr int kProfCap = 1024;
 void prof_mark(lmoe_ctx* ctx, int boundary, cudaStream_t st) {
   if (!ctx->prof_on || ctx->prof_calls >= kProfCap) return;
   cudaEventRecord(ctx->prof_ev[(size_t)ctx->prof_calls * (LMOE_NUM_STAGES + 1) + boundary], st);
+}
+
+// NVTX ranges of a forward: "lmoe_forward" around the call, one range per stage inside it
+// (host-side annotations that profilers align with the kernels each stage launches).
+const char* const kStageNames[LMOE_NUM_STAGES] = {
+    "router GEMM", "cutoff + top-K + segments", "W_down GEMM", "expert gate/up GEMM",
+    "expert down GEMM", "RMSNorm + combine", "shared gate/up GEMM", "W_up + shared down GEMM"};
+
+void nvtx_stage(lmoe_ctx* ctx, int boundary) {
+  if (ctx->nvtx_open == 0) return;        // not inside lmoe_forward (e.g. lmoe_route)
+  if (ctx->nvtx_open > 1) {
+    nvtxRangePop();
+    --ctx->nvtx_open;
+  }
+  if (boundary < LMOE_NUM_STAGES) {
+    nvtxRangePushA(kStageNames[boundary]);
+    ++ctx->nvtx_open;
+  }
+}
+
+void nvtx_end(lmoe_ctx* ctx) {
+  for (; ctx->nvtx_open > 0; --ctx->nvtx_open) nvtxRangePop();
+}
+
+// Stage boundary b of a forward: stage b-1 ends and stage b begins.
+void stage_mark(lmoe_ctx* ctx, int boundary, cudaStream_t st) {
+  prof_mark(ctx, boundary, st);
+  nvtx_stage(ctx, boundary);
+}
+
+// LMOE_LOG=1: one line on stderr for every failing call of the public API.
+lmoe_status logged(const char* fn, lmoe_status s) {
+  if (s != LMOE_OK) {
+    const char* v = getenv("LMOE_LOG");
+    if (v && v[0] == '1') fprintf(stderr, "lmoe: %s: %s\n", fn, lmoe_status_string(s));
+  }
+  return s;
+}
+
+// Test hook: the next workspace / staging allocation of the library fails (lmoe_debug_fail_next_alloc).
+std::atomic<int> g_fail_next_alloc{0};
+
+cudaError_t ws_malloc(void** p, size_t bytes) {
+  if (g_fail_next_alloc.exchange(0)) {
+    *p = nullptr;
+    return cudaErrorMemoryAllocation;
+  }
+  return cudaMalloc(p, bytes);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -176,7 +228,7 @@ cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, in
   g.op = kOpRouter;
   cudaError_t e = run_gemm(ctx, g, st);
   if (e != cudaSuccess) return e;
-  prof_mark(ctx, 1, st);
+  stage_mark(ctx, 1, st);
   RouteArgs r;
   r.logits = ctx->logits; r.logits_t = ctx->logits_t;
   r.bt = bt; r.n_experts = c.n_experts; r.top_k = c.top_k; r.tile_m = kTileM;
@@ -191,6 +243,19 @@ cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, in
   e = launch_route_tail(r, st);
   if (e == cudaSuccess && ctx->momentum > 0.0) ctx->state_valid = true;
   return e;
+}
+
+// Runs the segment validation on the index buffers of the last bt tokens routed, then
+// synchronises `st` and returns (and clears) the status word.
+lmoe_status validate_routing(lmoe_ctx* ctx, int bt, cudaStream_t st) {
+  const lmoe_config& c = ctx->cfg;
+  ctx->launches += 1;
+  if (launch_validate_segments(ctx->idx, ctx->counts, ctx->offsets, ctx->perm, ctx->inv, bt, c.top_k, c.n_experts,
+                               ctx->status, ctx->sm_count, st) != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
+  }
+  return lmoe_sync_status(ctx, st);
 }
 
 }  // namespace
@@ -298,7 +363,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   size_t o_cat = cv.take<char>(bt * ldc * ctx->esz);
   size_t o_tscale = cv.take<float>(bt * K);
   ctx->ws_bytes = cv.off;
-  if (cudaMalloc(&ctx->ws, ctx->ws_bytes) != cudaSuccess) {
+  if (ws_malloc(reinterpret_cast<void**>(&ctx->ws), ctx->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     delete ctx;
     return LMOE_ERR_OOM;
@@ -362,21 +427,21 @@ extern "C" {
 
 lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt, lmoe_stream stream,
                         lmoe_ctx** out) {
-  return create_impl(cfg, w, nullptr, max_bt, stream, out);
+  return logged("lmoe_create", create_impl(cfg, w, nullptr, max_bt, stream, out));
 }
 
 lmoe_status lmoe_create_fp8(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* experts,
                             int32_t max_bt, lmoe_stream stream, lmoe_ctx** out) {
   if (!experts) {
     if (out) *out = nullptr;
-    return LMOE_ERR_INVALID_ARG;
+    return logged("lmoe_create_fp8", LMOE_ERR_INVALID_ARG);
   }
-  return create_impl(cfg, w, experts, max_bt, stream, out);
+  return logged("lmoe_create_fp8", create_impl(cfg, w, experts, max_bt, stream, out));
 }
 
-lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream,
-                       int32_t* topk_idx, float* topk_w, int32_t* expert_counts, double* alpha,
-                       float* logits) {
+static lmoe_status route_entry(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream,
+                               int32_t* topk_idx, float* topk_w, int32_t* expert_counts, double* alpha,
+                               float* logits) {
   if (!ctx || bt < 0 || bt > ctx->max_bt) return LMOE_ERR_INVALID_ARG;
   if (bt == 0) return LMOE_OK;
   if (!x || !aligned16(x)) return LMOE_ERR_INVALID_ARG;
@@ -384,6 +449,10 @@ lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream str
   const lmoe_config& c = ctx->cfg;
   ctx->last_bt = bt;
   cudaError_t e = route_impl(ctx, x, bt, st, expert_counts);
+  if (e == cudaSuccess && ctx->check) {
+    const lmoe_status vs = validate_routing(ctx, bt, st);
+    if (vs != LMOE_OK) return vs;
+  }
   const size_t btK = (size_t)bt * c.top_k;
   if (e == cudaSuccess && topk_idx)
     e = cudaMemcpyAsync(topk_idx, ctx->idx, btK * 4, cudaMemcpyDeviceToDevice, st);
@@ -396,7 +465,7 @@ lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream str
   return finish(ctx, st, e);
 }
 
-lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream) {
+static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream) {
   if (!ctx || bt < 0 || bt > ctx->max_bt) return LMOE_ERR_INVALID_ARG;
   if (bt == 0) return LMOE_OK;
   if (!x || !out || !aligned16(x) || !aligned16(out)) return LMOE_ERR_INVALID_ARG;
@@ -407,9 +476,18 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
   if (ob < xb + xbytes && xb < ob + xbytes) return LMOE_ERR_INVALID_ARG;  // out overlaps x
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ctx->last_bt = bt;
-  prof_mark(ctx, 0, st);
+  nvtxRangePushA("lmoe_forward");
+  ctx->nvtx_open = 1;
+  stage_mark(ctx, 0, st);
   cudaError_t e = route_impl(ctx, x, bt, st, nullptr);
-  prof_mark(ctx, 2, st);
+  stage_mark(ctx, 2, st);
+  if (e == cudaSuccess && ctx->check) {  // check mode: the segments are verified before any kernel indexes through them
+    const lmoe_status vs = validate_routing(ctx, bt, st);
+    if (vs != LMOE_OK) {
+      nvtx_end(ctx);
+      return vs;
+    }
+  }
   const long long ldc = (long long)c.latent + (long long)c.n_shared * c.shared_inter;
   const int max_mtiles = (int)(((long long)bt * c.top_k) / kTileM + c.n_experts + 1);  // >= sum of ceil(cnt/kTileM)
 
@@ -421,7 +499,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     g.epi = kEpiStore; g.out = ctx->z; g.ldo = c.latent;
     g.op = kOpDown;
     e = run_gemm(ctx, g, st);
-    prof_mark(ctx, 3, st);
+    stage_mark(ctx, 3, st);
   }
   if (e == cudaSuccess) {  // h[slot] = act(W_g[e] z[perm[slot]], W_u[e] z[perm[slot]])
     GemmArgs g = base_args(ctx);
@@ -433,7 +511,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     g.epi = kEpiGlu; g.out = ctx->h; g.ldo = c.expert_inter;
     g.op = kOpExpertGateUp;
     e = run_gemm(ctx, g, st);
-    prof_mark(ctx, 4, st);
+    stage_mark(ctx, 4, st);
   }
   if (e == cudaSuccess) {  // y[slot] = W_d[e] h[slot]
     GemmArgs g = base_args(ctx);
@@ -445,7 +523,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     g.epi = kEpiStore; g.out = ctx->y; g.ldo = c.latent;
     g.op = kOpExpertDown;
     e = run_gemm(ctx, g, st);
-    prof_mark(ctx, 5, st);
+    stage_mark(ctx, 5, st);
   }
   if (e == cudaSuccess) {  // c = sum_k w RMSNorm(y_k) -> cat[:, 0:L]
     CombineArgs a;
@@ -455,7 +533,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     a.norm_sum = ctx->norm_sum;
     e = launch_combine(a, ctx->bf16, st);
     ctx->launches += 1;
-    prof_mark(ctx, 6, st);
+    stage_mark(ctx, 6, st);
   }
   if (e == cudaSuccess) {  // shared activations -> cat[:, L:]
     GemmArgs g = base_args(ctx);
@@ -467,7 +545,7 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     g.out = static_cast<char*>(ctx->cat) + (size_t)c.latent * ctx->esz; g.ldo = ldc;
     g.op = kOpSharedGateUp;
     e = run_gemm(ctx, g, st);
-    prof_mark(ctx, 7, st);
+    stage_mark(ctx, 7, st);
   }
   if (e == cudaSuccess) {  // out = [c | h_sh] [W_up | W_d^sh_0 | ...]^T
     GemmArgs g = base_args(ctx);
@@ -485,9 +563,10 @@ lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lm
     g.epi = kEpiStore; g.out = out; g.ldo = c.d;
     g.op = kOpFinal;
     e = run_gemm(ctx, g, st);
-    prof_mark(ctx, 8, st);
+    stage_mark(ctx, 8, st);
   }
   if (ctx->prof_on && ctx->prof_calls < kProfCap) ctx->prof_calls++;
+  nvtx_end(ctx);
   return finish(ctx, st, e);
 }
 
@@ -547,7 +626,7 @@ lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t*
   return LMOE_OK;
 }
 
-lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream) {
+static lmoe_status sync_status_entry(lmoe_ctx* ctx, lmoe_stream stream) {
   if (!ctx) return LMOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(st) != cudaSuccess) return LMOE_ERR_CUDA;
@@ -559,7 +638,8 @@ lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream) {
   return LMOE_OK;
 }
 
-lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host, lmoe_stream stream) {
+static lmoe_status forward_host_entry(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host,
+                                      lmoe_stream stream) {
   if (!ctx || bt < 0 || bt > ctx->max_bt) return LMOE_ERR_INVALID_ARG;
   if (bt == 0) return LMOE_OK;
   if (!x_host || !out_host) return LMOE_ERR_INVALID_ARG;
@@ -577,7 +657,7 @@ lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, voi
   }
   if (!ctx->host_ws) {  // first call: staging buffers, copy stream, events
     const size_t one = align_up((size_t)ctx->max_bt * ctx->cfg.d * ctx->esz, 256);
-    if (cudaMalloc(&ctx->host_ws, 3 * one) != cudaSuccess) {
+    if (ws_malloc(reinterpret_cast<void**>(&ctx->host_ws), 3 * one) != cudaSuccess) {
       cudaGetLastError();
       ctx->host_ws = nullptr;
       return LMOE_ERR_OOM;
@@ -608,7 +688,7 @@ lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, voi
     return LMOE_ERR_CUDA;
   }
   ctx->host_next = b ^ 1;
-  const lmoe_status s = lmoe_forward(ctx, xd, bt, od, stream);
+  const lmoe_status s = forward_entry(ctx, xd, bt, od, stream);
   if (s != LMOE_OK) return s;
   e = cudaEventRecord(ctx->host_used[b], st);
   // output copy in stream order: done when the caller's stream passes this call
@@ -629,6 +709,34 @@ void lmoe_destroy(lmoe_ctx* ctx) {
   cudaFree(ctx->ws);
   delete ctx;
 }
+
+lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream, int32_t* topk_idx,
+                       float* topk_w, int32_t* expert_counts, double* alpha, float* logits) {
+  nvtxRangePushA("lmoe_route");
+  const lmoe_status s = route_entry(ctx, x, bt, stream, topk_idx, topk_w, expert_counts, alpha, logits);
+  nvtxRangePop();
+  return logged("lmoe_route", s);
+}
+
+lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream) {
+  return logged("lmoe_forward", forward_entry(ctx, x, bt, out, stream));
+}
+
+lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host, lmoe_stream stream) {
+  return logged("lmoe_forward_host", forward_host_entry(ctx, x_host, bt, out_host, stream));
+}
+
+lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream) {
+  return logged("lmoe_sync_status", sync_status_entry(ctx, stream));
+}
+
+lmoe_status lmoe_debug_check_segments(lmoe_ctx* ctx, lmoe_stream stream) {
+  if (!ctx) return logged("lmoe_debug_check_segments", LMOE_ERR_INVALID_ARG);
+  if (ctx->last_bt == 0) return LMOE_OK;
+  return logged("lmoe_debug_check_segments", validate_routing(ctx, ctx->last_bt, static_cast<cudaStream_t>(stream)));
+}
+
+void lmoe_debug_fail_next_alloc(void) { g_fail_next_alloc.store(1); }
 
 lmoe_status lmoe_workspace(const lmoe_ctx* ctx, lmoe_workspace_view* v) {
   if (!ctx || !v) return LMOE_ERR_INVALID_ARG;

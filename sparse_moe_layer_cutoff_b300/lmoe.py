@@ -74,6 +74,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_forward.restype = c_i32
     lib.lmoe_forward_host.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
     lib.lmoe_forward_host.restype = c_i32
+    lib.lmoe_debug_check_segments.argtypes = [c_vp, c_vp]
+    lib.lmoe_debug_check_segments.restype = c_i32
+    lib.lmoe_debug_fail_next_alloc.argtypes = []
+    lib.lmoe_debug_fail_next_alloc.restype = None
     lib.lmoe_sync_status.argtypes = [c_vp, c_vp]
     lib.lmoe_sync_status.restype = c_i32
     lib.lmoe_destroy.argtypes = [c_vp]
@@ -148,6 +152,16 @@ def lmoe_forward(ctx, x: int, bt: int, out: int, stream: int = 0) -> int:
 def lmoe_forward_host(ctx, x_host: int, bt: int, out_host: int, stream: int = 0) -> int:
     """lmoe_forward with x and out in host memory (staged by the context)."""
     return load_library().lmoe_forward_host(c_vp(ctx), c_vp(x_host), bt, c_vp(out_host), c_vp(stream))
+
+
+def lmoe_debug_check_segments(ctx, stream: int = 0) -> int:
+    """Validate the routing index buffers of the context's last call (synchronises)."""
+    return load_library().lmoe_debug_check_segments(c_vp(ctx), c_vp(stream))
+
+
+def lmoe_debug_fail_next_alloc() -> None:
+    """Make the library's next workspace or staging allocation fail (one shot)."""
+    load_library().lmoe_debug_fail_next_alloc()
 
 
 def lmoe_sync_status(ctx, stream: int = 0) -> int:

@@ -2,10 +2,14 @@
 and rejects bad arguments on the host before touching the GPU.  CPU only."""
 import ctypes
 import os
+import subprocess
+import sys
 
 import pytest
 
 from sparse_moe_layer_cutoff_b300 import lmoe as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 @pytest.fixture(scope="module")
@@ -89,3 +93,22 @@ def test_calls_on_null_context(lib):
     with pytest.raises(L.LmoeError):
         L.lmoe_workspace(None)
     L.lmoe_destroy(None)   # no-op
+
+
+def _create_null_cfg(env):
+    code = ("import ctypes; from sparse_moe_layer_cutoff_b300 import lmoe as L; out = ctypes.c_void_p(); "
+            "print(L.load_library().lmoe_create(None, None, 8, None, ctypes.byref(out)))")
+    return subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=120,
+                          cwd=ROOT)
+
+
+def test_log_env_reports_failing_calls():
+    """LMOE_LOG=1: a failing call (here a NULL config, rejected before any CUDA call) prints one
+    line on stderr; without it the library prints nothing."""
+    env = dict(os.environ, LMOE_LOG="1")
+    r = _create_null_cfg(env)
+    assert r.returncode == 0 and r.stdout.strip() == str(L.LMOE_ERR_INVALID_ARG)
+    assert "lmoe: lmoe_create: " in r.stderr
+    env.pop("LMOE_LOG")
+    r = _create_null_cfg(env)
+    assert r.returncode == 0 and "lmoe:" not in r.stderr

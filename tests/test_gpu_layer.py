@@ -403,3 +403,58 @@ def test_forward_host_argument_errors():
         layer.forward_host(x)
     assert layer.sync_status() == 0
     layer.close()
+
+
+def test_check_mode_validates_routing_indices(monkeypatch):
+    """LMOE_CHECK=1 validates the expert segments after routing and before any kernel indexes
+    through them; the output keeps the unchecked layer's bits.  A corrupted perm (two slots of
+    one expert's segment swapped, so inv no longer inverts it) is reported by
+    lmoe_debug_check_segments as LMOE_ERR_DEVICE_ASSERT; no forward runs on it, and the next
+    route rewrites the buffers."""
+    wl = WORKLOADS["small_bf16"]
+    x, weights, bias = make_inputs(wl, "cuda", 300)
+    plain = LatentMoE(SMALL, weights, max_bt=300, router_bias=bias)
+    want = plain.forward(x).clone()
+    torch.cuda.synchronize()
+    plain.close()
+    monkeypatch.setenv("LMOE_CHECK", "1")
+    layer = LatentMoE(SMALL, weights, max_bt=300, router_bias=bias)
+    assert torch.equal(layer.forward(x), want)
+    assert L.lmoe_debug_check_segments(layer.ctx) == L.LMOE_OK
+    ws = workspace_tensors(layer)
+    off = ws["offsets"].cpu().numpy()
+    e = int(np.argmax(np.diff(off) >= 2))
+    a, b = int(off[e]), int(off[e]) + 1           # two slots of expert e: two different tokens
+    perm = ws["perm"]
+    perm[[a, b]] = perm[[b, a]].clone()
+    torch.cuda.synchronize()
+    assert L.lmoe_debug_check_segments(layer.ctx) == L.LMOE_ERR_DEVICE_ASSERT
+    assert L.lmoe_debug_check_segments(layer.ctx) == L.LMOE_ERR_DEVICE_ASSERT
+    layer.route(x)
+    torch.cuda.synchronize()
+    assert L.lmoe_debug_check_segments(layer.ctx) == L.LMOE_OK
+    assert torch.equal(layer.forward(x), want)
+    layer.close()
+
+
+def test_injected_allocation_failure_returns_oom():
+    """lmoe_debug_fail_next_alloc: the next workspace allocation fails and the call returns
+    LMOE_ERR_OOM; the hook is one-shot, so the following create works; the same for the
+    staging buffers of the first host-buffer forward."""
+    wl = WORKLOADS["small_bf16"]
+    x, weights, bias = make_inputs(wl, "cuda", 64)
+    L.lmoe_debug_fail_next_alloc()
+    with pytest.raises(LmoeError) as ei:
+        LatentMoE(SMALL, weights, max_bt=64, router_bias=bias)
+    assert ei.value.status == L.LMOE_ERR_OOM
+    layer = LatentMoE(SMALL, weights, max_bt=64, router_bias=bias)
+    xh = x.cpu().pin_memory()
+    L.lmoe_debug_fail_next_alloc()
+    with pytest.raises(LmoeError) as ei:
+        layer.forward_host(xh)
+    assert ei.value.status == L.LMOE_ERR_OOM
+    got = layer.forward_host(xh)
+    torch.cuda.synchronize()
+    assert torch.equal(got, layer.forward(x).cpu())
+    assert layer.sync_status() == 0
+    layer.close()
