@@ -73,6 +73,9 @@ WORKLOADS = {
     # profiling case for counter captures: the full-width kernels with 32 experts (2.5 GB of
     # weights, still far above L2) and ~148 tokens per expert, as at bt = 8192 with 896
     "profile_e32_bt296": Workload("profile_e32_bt296", dataclasses.replace(FULL, n_experts=32), 296, 5),
+    # profiling case for the token-row kernels (gather, RMSNorm + combine): 2048 tokens x 16
+    # expert rows of latent 3584 are 235 MB per pass, above the 126 MB L2, as at bt = 8192
+    "profile_e32_bt2048": Workload("profile_e32_bt2048", dataclasses.replace(FULL, n_experts=32), 2048, 6),
 }
 
 
