@@ -193,9 +193,20 @@ void release_host_io(lmoe_ctx* ctx) {
   ctx->host_next = 0;
 }
 
+// Synchronise `st`, then read and clear the context's device status word.
+lmoe_status read_status(lmoe_ctx* ctx, cudaStream_t st) {
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LMOE_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, ctx->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (v && cudaMemset(ctx->status, 0, 4) != cudaSuccess) return LMOE_ERR_CUDA;
+  if (v & kStatusTimeout) return LMOE_ERR_TIMEOUT;
+  if (v & kStatusAssert) return LMOE_ERR_DEVICE_ASSERT;
+  return LMOE_OK;
+}
+
 lmoe_status finish(lmoe_ctx* ctx, cudaStream_t st, cudaError_t e) {
   if (e != cudaSuccess) return LMOE_ERR_CUDA;
-  if (ctx->check) return lmoe_sync_status(ctx, st);
+  if (ctx->check) return read_status(ctx, st);
   return LMOE_OK;
 }
 
@@ -255,7 +266,7 @@ lmoe_status validate_routing(lmoe_ctx* ctx, int bt, cudaStream_t st) {
     cudaGetLastError();
     return LMOE_ERR_CUDA;
   }
-  return lmoe_sync_status(ctx, st);
+  return read_status(ctx, st);
 }
 
 }  // namespace
@@ -628,14 +639,7 @@ lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t*
 
 static lmoe_status sync_status_entry(lmoe_ctx* ctx, lmoe_stream stream) {
   if (!ctx) return LMOE_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (cudaStreamSynchronize(st) != cudaSuccess) return LMOE_ERR_CUDA;
-  uint32_t v = 0;
-  if (cudaMemcpy(&v, ctx->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return LMOE_ERR_CUDA;
-  if (v && cudaMemset(ctx->status, 0, 4) != cudaSuccess) return LMOE_ERR_CUDA;
-  if (v & kStatusTimeout) return LMOE_ERR_TIMEOUT;
-  if (v & kStatusAssert) return LMOE_ERR_DEVICE_ASSERT;
-  return LMOE_OK;
+  return read_status(ctx, static_cast<cudaStream_t>(stream));
 }
 
 static lmoe_status forward_host_entry(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host,
