@@ -368,12 +368,14 @@ def main(argv=None):
     ap.add_argument("--cpu-tokens", type=int, default=12, help="oracle sample for cpu_baseline")
     ap.add_argument("--cpu-tokens-ref", type=int, default=2, help="oracle sample per reference step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=None, help="default: --steps")
     ap.add_argument("--fp8-experts", action="store_true",
                     help="routed experts in e4m3 (lmoe_create_fp8); a separate line, not the bf16 headline")
     ap.add_argument("--latent-norm", default="expert", choices=["expert", "combined"],
                     help="latent RMSNorm placement; 'combined' (one norm of the weighted sum) is a separate line")
     args = ap.parse_args(argv)
+    if args.e2e_steps is None:
+        args.e2e_steps = args.steps
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_setup()
@@ -523,7 +525,7 @@ def main(argv=None):
                 "cpu_baseline": cpu,
                 "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": xbytes,
                         "d2h_bytes_per_step": xbytes, "api": "lmoe_forward_host, pinned host buffers",
-                        "timer": "wall clock, device synchronised on both sides"},
+                        "timer": "wall clock, device synchronised on both sides", "steps": args.e2e_steps},
                 "gpu_launches": launches, "clocks": clk, "engine": lmoe_build_info()}
         if args.fp8_experts:
             line["dtype"] = "bf16 (routed experts e4m3)"

@@ -144,15 +144,18 @@ LMOE_API lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream);
 /* lmoe_forward with the input and output in host memory: x_host [bt, d] and out_host [bt, d],
  * both of cfg.dtype, page-locked (cudaHostAlloc / cudaHostRegister) for copies that overlap
  * the GPU's work, or pageable (then each copy also stalls the calling thread).  The context
- * stages them through device buffers it owns (3 x max_bt x d elements, allocated by the first
- * call, which therefore synchronises the device and cannot be captured in a CUDA graph).
- * The input copy runs on an internal copy stream into one of two staging buffers, so it
- * overlaps the previous call's forward; it reads x_host at some point after the call is made,
- * so x_host must already hold the input when lmoe_forward_host is called and stay unchanged
- * until `stream` passes the call.  The forward and the output copy run on `stream`: out_host
- * is written when `stream` passes the call.  Errors: as lmoe_forward; LMOE_ERR_INVALID_ARG
- * also for device or managed pointers and overlapping x_host / out_host; LMOE_ERR_OOM if the
- * staging buffers cannot be allocated. */
+ * stages them through device buffers it owns (two inputs and two outputs of max_bt x d
+ * elements, allocated by the first call, which therefore synchronises the device and cannot be
+ * captured in a CUDA graph).  The input copy, the forward and the output copy each run on an
+ * internal stream of the context, so in a sequence of calls the input copy of the next call and
+ * the output copy of the previous one overlap the current forward.  `stream` waits for this
+ * call's output copy: out_host is written when `stream` passes the call.  The call does not
+ * wait for earlier work on `stream` (its inputs are host memory), except for this context's own
+ * device-buffer calls, which are ordered with its forwards internally (they share the context's
+ * workspace).  x_host is read at some point after the call is made, so it must already hold the
+ * input and stay unchanged until `stream` passes the call.  Errors: as lmoe_forward;
+ * LMOE_ERR_INVALID_ARG also for device or managed pointers and overlapping x_host / out_host;
+ * LMOE_ERR_OOM if the staging buffers cannot be allocated. */
 LMOE_API lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host,
                                        lmoe_stream stream);
 

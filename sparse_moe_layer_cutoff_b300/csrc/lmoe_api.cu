@@ -63,10 +63,15 @@ struct lmoe_ctx {
   long long launches;
   long long prof_launch_base;
   // host-buffer entry point (created by its first call)
-  char* host_ws;             // two x staging buffers, then one out buffer, [max_bt, d] each
-  cudaStream_t host_cs;      // copy stream of the input copies
-  cudaEvent_t host_in[2];    // input copy into staging buffer b done
-  cudaEvent_t host_used[2];  // the forward that read staging buffer b done
+  char* host_ws;               // staging buffers x[0], x[1], out[0], out[1], [max_bt, d] each
+  cudaStream_t host_in_st;     // input copies
+  cudaStream_t host_run_st;    // forwards of host-buffer calls
+  cudaStream_t host_out_st;    // output copies
+  cudaEvent_t host_in[2];      // input copy into x[b] done
+  cudaEvent_t host_run[2];     // forward of the call that used x[b] and out[b] done
+  cudaEvent_t host_out[2];     // output copy from out[b] done
+  cudaEvent_t host_last_run;   // the last host-buffer forward done
+  cudaEvent_t host_dev_done;   // the last device-buffer call's work done
   int host_next;
   int nvtx_open;             // NVTX ranges this forward has pushed and not yet popped
 };
@@ -179,18 +184,31 @@ struct Carve {
   }
 };
 
-// Staging buffers, copy stream and events of lmoe_forward_host (no-op if never created).
+// Staging buffers, streams and events of lmoe_forward_host (no-op if never created).
 void release_host_io(lmoe_ctx* ctx) {
-  for (int b = 0; b < 2; ++b) {
-    if (ctx->host_in[b]) cudaEventDestroy(ctx->host_in[b]);
-    if (ctx->host_used[b]) cudaEventDestroy(ctx->host_used[b]);
-    ctx->host_in[b] = ctx->host_used[b] = nullptr;
+  for (cudaEvent_t* ev : {&ctx->host_in[0], &ctx->host_in[1], &ctx->host_run[0], &ctx->host_run[1],
+                          &ctx->host_out[0], &ctx->host_out[1], &ctx->host_last_run, &ctx->host_dev_done}) {
+    if (*ev) cudaEventDestroy(*ev);
+    *ev = nullptr;
   }
-  if (ctx->host_cs) cudaStreamDestroy(ctx->host_cs);
-  ctx->host_cs = nullptr;
+  for (cudaStream_t* st : {&ctx->host_in_st, &ctx->host_run_st, &ctx->host_out_st}) {
+    if (*st) cudaStreamDestroy(*st);
+    *st = nullptr;
+  }
   cudaFree(ctx->host_ws);
   ctx->host_ws = nullptr;
   ctx->host_next = 0;
+}
+
+// Device-buffer calls share the context's workspace with the host-buffer forwards, which run on
+// the context's own stream: once lmoe_forward_host has been used, a device-buffer call waits for
+// the last host-buffer forward and marks where its own work ends (for the next host-buffer one).
+void host_order_begin(lmoe_ctx* ctx, cudaStream_t st) {
+  if (ctx && ctx->host_ws) cudaStreamWaitEvent(st, ctx->host_last_run, 0);
+}
+
+void host_order_end(lmoe_ctx* ctx, cudaStream_t st) {
+  if (ctx && ctx->host_ws) cudaEventRecord(ctx->host_dev_done, st);
 }
 
 // Synchronise `st`, then read and clear the context's device status word.
@@ -659,44 +677,54 @@ static lmoe_status forward_host_entry(lmoe_ctx* ctx, const void* x_host, int32_t
     }
     if (at.type != cudaMemoryTypeHost && at.type != cudaMemoryTypeUnregistered) return LMOE_ERR_INVALID_ARG;
   }
-  if (!ctx->host_ws) {  // first call: staging buffers, copy stream, events
-    const size_t one = align_up((size_t)ctx->max_bt * ctx->cfg.d * ctx->esz, 256);
-    if (ws_malloc(reinterpret_cast<void**>(&ctx->host_ws), 3 * one) != cudaSuccess) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t one = align_up((size_t)ctx->max_bt * ctx->cfg.d * ctx->esz, 256);
+  if (!ctx->host_ws) {  // first call: staging buffers, streams, events
+    if (ws_malloc(reinterpret_cast<void**>(&ctx->host_ws), 4 * one) != cudaSuccess) {
       cudaGetLastError();
       ctx->host_ws = nullptr;
       return LMOE_ERR_OOM;
     }
-    bool ok = cudaStreamCreateWithFlags(&ctx->host_cs, cudaStreamNonBlocking) == cudaSuccess;
-    for (int b = 0; b < 2 && ok; ++b)
-      ok = cudaEventCreateWithFlags(&ctx->host_in[b], cudaEventDisableTiming) == cudaSuccess &&
-           cudaEventCreateWithFlags(&ctx->host_used[b], cudaEventDisableTiming) == cudaSuccess;
+    bool ok = true;
+    for (cudaStream_t* s2 : {&ctx->host_in_st, &ctx->host_run_st, &ctx->host_out_st})
+      ok = ok && cudaStreamCreateWithFlags(s2, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* ev : {&ctx->host_in[0], &ctx->host_in[1], &ctx->host_run[0], &ctx->host_run[1],
+                            &ctx->host_out[0], &ctx->host_out[1], &ctx->host_last_run, &ctx->host_dev_done})
+      ok = ok && cudaEventCreateWithFlags(ev, cudaEventDisableTiming) == cudaSuccess;
+    // the device-buffer calls made so far were on the caller's stream
+    ok = ok && cudaEventRecord(ctx->host_dev_done, st) == cudaSuccess;
     if (!ok) {
       cudaGetLastError();
       release_host_io(ctx);
       return LMOE_ERR_CUDA;
     }
   }
-  const size_t one = align_up((size_t)ctx->max_bt * ctx->cfg.d * ctx->esz, 256);
   const int b = ctx->host_next;
   char* xd = ctx->host_ws + (size_t)b * one;
-  char* od = ctx->host_ws + 2 * one;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // input copy on the copy stream, once the forward that last read this staging buffer is done;
-  // it overlaps whatever runs on the caller's stream before this call (the previous forward)
-  cudaError_t e = cudaStreamWaitEvent(ctx->host_cs, ctx->host_used[b], 0);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, ctx->host_cs);
-  if (e == cudaSuccess) e = cudaEventRecord(ctx->host_in[b], ctx->host_cs);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->host_in[b], 0);
+  char* od = ctx->host_ws + (size_t)(2 + b) * one;
+  // input copy once the forward that last read x[b] is done; it overlaps the previous forward
+  cudaError_t e = cudaStreamWaitEvent(ctx->host_in_st, ctx->host_run[b], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, ctx->host_in_st);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->host_in[b], ctx->host_in_st);
+  // forward once its input is in, the output copy that last read out[b] is done, and the last
+  // device-buffer call on this context is done
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->host_run_st, ctx->host_in[b], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->host_run_st, ctx->host_out[b], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->host_run_st, ctx->host_dev_done, 0);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return LMOE_ERR_CUDA;
   }
   ctx->host_next = b ^ 1;
-  const lmoe_status s = forward_entry(ctx, xd, bt, od, stream);
+  const lmoe_status s = forward_entry(ctx, xd, bt, od, ctx->host_run_st);
   if (s != LMOE_OK) return s;
-  e = cudaEventRecord(ctx->host_used[b], st);
-  // output copy in stream order: done when the caller's stream passes this call
-  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, st);
+  e = cudaEventRecord(ctx->host_run[b], ctx->host_run_st);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->host_last_run, ctx->host_run_st);
+  // output copy on its own stream (it overlaps the next forward); the caller's stream waits for it
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->host_out_st, ctx->host_run[b], 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out_host, od, bytes, cudaMemcpyDeviceToHost, ctx->host_out_st);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->host_out[b], ctx->host_out_st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->host_out[b], 0);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return LMOE_ERR_CUDA;
@@ -717,13 +745,18 @@ void lmoe_destroy(lmoe_ctx* ctx) {
 lmoe_status lmoe_route(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream, int32_t* topk_idx,
                        float* topk_w, int32_t* expert_counts, double* alpha, float* logits) {
   nvtxRangePushA("lmoe_route");
+  host_order_begin(ctx, static_cast<cudaStream_t>(stream));
   const lmoe_status s = route_entry(ctx, x, bt, stream, topk_idx, topk_w, expert_counts, alpha, logits);
+  host_order_end(ctx, static_cast<cudaStream_t>(stream));
   nvtxRangePop();
   return logged("lmoe_route", s);
 }
 
 lmoe_status lmoe_forward(lmoe_ctx* ctx, const void* x, int32_t bt, void* out, lmoe_stream stream) {
-  return logged("lmoe_forward", forward_entry(ctx, x, bt, out, stream));
+  host_order_begin(ctx, static_cast<cudaStream_t>(stream));
+  const lmoe_status s = forward_entry(ctx, x, bt, out, stream);
+  host_order_end(ctx, static_cast<cudaStream_t>(stream));
+  return logged("lmoe_forward", s);
 }
 
 lmoe_status lmoe_forward_host(lmoe_ctx* ctx, const void* x_host, int32_t bt, void* out_host, lmoe_stream stream) {
@@ -737,6 +770,7 @@ lmoe_status lmoe_sync_status(lmoe_ctx* ctx, lmoe_stream stream) {
 lmoe_status lmoe_debug_check_segments(lmoe_ctx* ctx, lmoe_stream stream) {
   if (!ctx) return logged("lmoe_debug_check_segments", LMOE_ERR_INVALID_ARG);
   if (ctx->last_bt == 0) return LMOE_OK;
+  host_order_begin(ctx, static_cast<cudaStream_t>(stream));
   return logged("lmoe_debug_check_segments", validate_routing(ctx, ctx->last_bt, static_cast<cudaStream_t>(stream)));
 }
 

@@ -458,3 +458,34 @@ def test_injected_allocation_failure_returns_oom():
     assert torch.equal(got, layer.forward(x).cpu())
     assert layer.sync_status() == 0
     layer.close()
+
+
+def test_forward_host_and_device_calls_interleave():
+    """Host-buffer forwards run on the context's own streams; device-buffer calls on the same
+    context (which share its workspace) are ordered with them: an unsynchronised mix of both
+    kinds, with a route call among them, gives every call its own bits."""
+    wl = WORKLOADS["small_bf16"]
+    x0, weights, bias = make_inputs(wl, "cuda", 300)
+    xs = [x0] + [make_x(wl, "cuda", 300, seed_offset=k) for k in (6, 7, 8, 9, 10)]
+    layer = LatentMoE(SMALL, weights, max_bt=300, router_bias=bias)
+    want = [layer.forward(x).clone() for x in xs]
+    want_idx = layer.route(xs[3])["idx"].clone()
+    torch.cuda.synchronize()
+    hx = [x.cpu().pin_memory() for x in xs]
+    ho = [torch.empty_like(h).pin_memory() for h in hx]
+    dout = [torch.empty_like(x) for x in xs]
+    r3 = None
+    for i in range(len(xs)):
+        if i % 2 == 0:
+            layer.forward_host(hx[i], ho[i])
+        else:
+            layer.forward(xs[i], dout[i])
+            if i == 3:
+                r3 = layer.route(xs[i])
+    torch.cuda.synchronize()
+    for i in range(len(xs)):
+        got = ho[i] if i % 2 == 0 else dout[i].cpu()
+        assert torch.equal(got, want[i].cpu()), i
+    assert torch.equal(r3["idx"], want_idx)
+    assert layer.sync_status() == 0
+    layer.close()
