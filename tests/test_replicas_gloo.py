@@ -35,7 +35,7 @@ def test_two_replicas_reduce_time_and_tokens():
     if torch.cuda.is_available():
         pytest.skip("CPU gloo test")
     world, port = 2, _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()   # no fork of this (multi-threaded) process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, port, out), nprocs=world, join=True)
     assert out[0] == out[1] == (11.0, 300.0)
