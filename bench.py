@@ -371,6 +371,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=None, help="default: --steps")
     ap.add_argument("--fp8-experts", action="store_true",
                     help="routed experts in e4m3 (lmoe_create_fp8); a separate line, not the bf16 headline")
+    ap.add_argument("--bt", type=int, default=None,
+                    help="tokens per step instead of the workload's (same shape and recipe); a separate line")
     ap.add_argument("--latent-norm", default="expert", choices=["expert", "combined"],
                     help="latent RMSNorm placement; 'combined' (one norm of the weighted sum) is a separate line")
     args = ap.parse_args(argv)
@@ -392,6 +394,10 @@ def main(argv=None):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     w = WORKLOADS[args.workload]
+    if args.bt is not None:
+        if args.bt <= 0:
+            ap.error("--bt must be positive")
+        w = w.with_(bt=args.bt, name=f"{w.name} at bt={args.bt}")
     s = w.shape
     x, weights, bias = make_inputs(w, device)
     xs = [x, make_x(w, device, seed_offset=1 + rank)]
