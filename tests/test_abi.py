@@ -93,6 +93,32 @@ def test_calls_on_null_context(lib):
     with pytest.raises(L.LmoeError):
         L.lmoe_workspace(None)
     L.lmoe_destroy(None)   # no-op
+    assert L.lmoe_forward_host(None, 0x1000, 4, 0x2000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_set_latent_norm(None, L.LMOE_NORM_COMBINED) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_set_cutoff_momentum(None, 0.5) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_debug_check_segments(None) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_debug_inject_wait_timeout(None) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_profile(None, True) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_profile_read(None)[0] == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_ffn_forward(None, 0x1000, 4, 0x2000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_ffn_sync_status(None) == L.LMOE_ERR_INVALID_ARG
+    L.lmoe_ffn_destroy(None)   # no-op
+
+
+def test_host_side_argument_checks_of_the_widened_calls(lib):
+    """Rejected on the host before any CUDA call: bad dense-FFN configs, negative or zero-row
+    quantization requests."""
+    for cfg, status in [(L.lmoe_ffn_config(0, 2048, 4.0, 25.0), L.LMOE_ERR_INVALID_ARG),
+                        (L.lmoe_ffn_config(1024, 2048, 0.0, 25.0), L.LMOE_ERR_INVALID_ARG),
+                        (L.lmoe_ffn_config(1000, 2048, 4.0, 25.0), L.LMOE_ERR_UNSUPPORTED),
+                        (L.lmoe_ffn_config(1024, 2000, 4.0, 25.0), L.LMOE_ERR_UNSUPPORTED)]:
+        st, ffn = L.lmoe_ffn_create(cfg, 0x10000, 0x10000, 0x10000, 64)
+        assert st == status and not ffn
+    st, ffn = L.lmoe_ffn_create(L.lmoe_ffn_config(1024, 2048, 4.0, 25.0), 0x10000, 0x10000, 0x10000, 0)
+    assert st == L.LMOE_ERR_INVALID_ARG and not ffn
+    assert L.lmoe_quantize_fp8_rows(0x10000, -1, 16, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_quantize_fp8_rows(0x10000, 4, 0, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_quantize_fp8_rows(0x10000, 0, 16, 0x20000, 0x30000) == L.LMOE_OK
 
 
 def _create_null_cfg(env):
