@@ -475,6 +475,30 @@ def test_zipf_and_repeated_block_recipe():
     np.testing.assert_allclose(ranks.numpy(), 3.0 * np.arange(1, 17, dtype=np.float64) ** -1.1, rtol=1e-6)
 
 
+def test_input_recipe_scales():
+    """Reading A18: x ~ N(0, 1), router weights std 0.02, every other weight std 1/sqrt(fan_in)
+    ([out, in] row-major, fan_in = in), gamma = 1 (1 + N(0, 0.1^2) with gamma noise); checked
+    on the small bf16 workload against the sampling error of each tensor's standard deviation."""
+    w = WORKLOADS["small_bf16"]
+    s = w.shape
+    x, W, bias = make_inputs(w, "cpu")
+    assert bias is None and x.dtype == torch.bfloat16 and x.shape == (w.bt, s.d)
+
+    def check(t, std):
+        v = t.float().flatten()
+        n = v.numel()
+        assert abs(float(v.mean())) < 5 * std / math.sqrt(n)
+        assert abs(float(v.std()) / std - 1.0) < 5 / math.sqrt(2 * n) + 4e-3   # + bf16 rounding
+
+    check(x, 1.0)
+    check(W["w_router"], 0.02)
+    for name in ("w_down", "exp_gate", "exp_up", "exp_down", "w_up", "sh_gate", "sh_up", "sh_down"):
+        check(W[name], 1.0 / math.sqrt(W[name].shape[-1]))
+    assert torch.all(W["latent_gamma"].float() == 1.0)
+    _, Wn, _ = make_inputs(w.with_(gamma_noise=0.1, bt=4), "cpu")
+    check(Wn["latent_gamma"].float() - 1.0, 0.1)
+
+
 # ----------------------------------------------------------------- dense first-layer FFN
 
 def test_dense_ffn_matches_torch_library_formulation():
