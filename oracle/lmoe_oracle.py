@@ -334,6 +334,15 @@ def bf16_round(v) -> np.ndarray:
     return r.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def quantize_activation_fp8(a, beta: float, beta_u: float) -> np.ndarray:
+    """The fp8 experts' activation h as the down projection reads it: every element of
+    a = SiTU-GLU(...) rounded to e4m3 after one fixed scale r = 448 / (beta * beta_u) taken
+    from the SiTU-GLU bound ([K3-news] ¶"第一": the bounded output is what makes fp8 safe), and
+    read back with s_h = (beta * beta_u) / 448.  The same scale for every token and feature."""
+    r, s_h = h_scales(beta, beta_u)
+    return round_e4m3(np.asarray(a, np.float64) * np.float64(r)) * np.float64(s_h)
+
+
 def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weights_fp8, gamma, beta: float,
                       beta_u: float, eps: float, norm: str = "expert") -> np.ndarray:
     """routed_latent with fp8 experts: z (the bf16 values the layer stores) quantized per
@@ -344,7 +353,6 @@ def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weight
     n, latent = z.shape
     zq, zs = quantize_rows_e4m3(z)
     zd = zq * zs[:, None].astype(np.float64)
-    r, s_h = h_scales(beta, beta_u)
     c = np.zeros((n, latent))
     gamma = _f64(gamma)
     for e in np.unique(idx):
@@ -355,8 +363,7 @@ def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weight
         wd = dq * np.asarray(ds, np.float64)[:, None]
         zr = zd[rows]
         a = situ_glu(zr @ wg.T, zr @ wu.T, beta, beta_u)
-        hq = round_e4m3(a * np.float64(r)) * np.float64(s_h)
-        y = hq @ wd.T
+        y = quantize_activation_fp8(a, beta, beta_u) @ wd.T
         term = rms_norm(y, gamma, eps) if norm == "expert" else y
         c[rows] += _f64(w)[rows, ks][:, None] * term
     return rms_norm(c, gamma, eps) if norm == "combined" else c

@@ -149,3 +149,41 @@ def test_dropped_latent_norm_is_caught(monkeypatch):
     monkeypatch.setattr(O, "rms_norm", lambda y, gamma, eps=1e-6: np.asarray(y, np.float64))
     assert _fails(P.test_norm_placements_unit_rms_and_single_expert)
     assert _fails(P.test_forward_combined_norm_matches_brute_force)
+
+
+def test_router_bias_subtracted_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "router_logits", lambda x, wr, bias=None:
+                        np.asarray(x, np.float64) @ np.asarray(wr, np.float64).T -
+                        (0.0 if bias is None else np.asarray(bias, np.float64)[None, :]))
+    assert _fails(P.test_router_logits_match_linear_and_per_element_loop)
+
+
+def test_router_bias_dropped_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "router_logits", lambda x, wr, bias=None:
+                        np.asarray(x, np.float64) @ np.asarray(wr, np.float64).T)
+    assert _fails(P.test_router_logits_match_linear_and_per_element_loop)
+
+
+def test_fp8_activation_left_unquantized_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "quantize_activation_fp8", lambda a, beta, beta_u: np.asarray(a, np.float64))
+    assert _fails(P.test_fp8_activation_quantization_per_element)
+    assert _fails(P.test_fp8_routed_latent_matches_brute_force)
+
+
+def test_fp8_activation_per_token_scale_is_caught(monkeypatch):
+    def per_token(a, beta, beta_u):
+        a = np.asarray(a, np.float64)
+        amax = np.abs(a).max(axis=-1, keepdims=True)
+        s = np.where(amax > 0, amax / 448.0, 1.0)
+        return O.round_e4m3(a / s) * s
+    monkeypatch.setattr(O, "quantize_activation_fp8", per_token)
+    assert _fails(P.test_fp8_activation_quantization_per_element)
+    assert _fails(P.test_fp8_routed_latent_matches_brute_force)
+
+
+def test_fp8_activation_scale_from_gate_bound_only_is_caught(monkeypatch):
+    # scale 448 / beta (the gate's bound alone) instead of 448 / (beta * beta_u)
+    monkeypatch.setattr(O, "quantize_activation_fp8", lambda a, beta, beta_u:
+                        O.round_e4m3(np.asarray(a, np.float64) * (448.0 / beta)) * (beta / 448.0))
+    assert _fails(P.test_fp8_activation_quantization_per_element)
+    assert _fails(P.test_fp8_routed_latent_matches_brute_force)

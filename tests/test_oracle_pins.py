@@ -587,3 +587,141 @@ def test_fp8_routed_latent_is_close_to_bf16_one():
     assert 1e-3 < rel < 0.08, rel
     rh, sh = O.h_scales(s.beta, s.beta_u)
     assert float(rh) * s.beta * s.beta_u <= 448.0 * (1 + 1e-6) and abs(float(rh) * float(sh) - 1.0) < 1e-6
+
+
+# ----------------------------------------------------------------- router logits
+
+def test_router_logits_match_linear_and_per_element_loop():
+    """l = x W_r^T + b ([K3-arch] step c: every token scored against every expert at model
+    width) against torch's fp64 linear (a library routine) and an explicit per-element sum,
+    on a non-square router with a non-zero bias of both signs; without a bias it is x W_r^T."""
+    rng = np.random.default_rng(21)
+    bt, d, E = 5, 7, 3
+    x = rng.normal(size=(bt, d))
+    wr = rng.normal(size=(E, d))
+    b = np.array([0.75, -1.5, 2.25])
+    got = O.router_logits(x, wr, b)
+    lib = F.linear(torch.from_numpy(x), torch.from_numpy(wr), torch.from_numpy(b)).numpy()
+    np.testing.assert_allclose(got, lib, rtol=1e-14, atol=1e-14)
+    loop = np.array([[sum(x[t][i] * wr[e][i] for i in range(d)) + b[e] for e in range(E)] for t in range(bt)])
+    np.testing.assert_allclose(got, loop, rtol=1e-14, atol=1e-14)
+    nob = F.linear(torch.from_numpy(x), torch.from_numpy(wr)).numpy()
+    np.testing.assert_allclose(O.router_logits(x, wr), nob, rtol=1e-14, atol=1e-14)
+    assert got.shape == (bt, E)
+
+
+# ----------------------------------------------------------------- fp8 activation, per element
+
+def _e4m3_table():
+    """Every finite e4m3 value with its code, decoded by torch from the 256 bit patterns
+    (a library routine), sorted by value."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    table = sorted((float(v), int(c)) for v, c in zip(vals, codes.numpy()) if np.isfinite(v) and not
+                   (v == 0 and int(c) == 0x80))
+    return table
+
+
+_E4M3 = None
+
+
+def _e4m3_nearest(v: float) -> float:
+    """Nearest finite e4m3 value by search over the decoded table: the closer neighbour, on an
+    exact tie the one whose code has an even mantissa (its lowest bit 0), and +-448 beyond the
+    range (the saturating reading)."""
+    global _E4M3
+    if _E4M3 is None:
+        _E4M3 = _e4m3_table()
+    import bisect
+    vals = [t[0] for t in _E4M3]
+    if v >= 448.0:
+        return 448.0
+    if v <= -448.0:
+        return -448.0
+    i = bisect.bisect_left(vals, v)
+    if i < len(vals) and vals[i] == v:
+        return v
+    lo, hi = _E4M3[i - 1], _E4M3[i]
+    dl, dh = v - lo[0], hi[0] - v
+    if dl < dh:
+        return lo[0]
+    if dh < dl:
+        return hi[0]
+    return lo[0] if (lo[1] & 1) == 0 else hi[0]
+
+
+def test_fp8_activation_quantization_per_element():
+    """Every element of the fp8 experts' activation is e4m3(a * 448 / (beta * beta_u)) read back
+    times (beta * beta_u) / 448: one fixed scale from the SiTU-GLU bound ([K3-news] ¶"第一"), the
+    same for every token and feature.  Checked element by element against the table search,
+    on activations spanning the whole range of the bounded SiTU-GLU, per-row magnitudes that
+    differ by orders of magnitude, and exact zeros."""
+    rng = np.random.default_rng(22)
+    beta, beta_u = 4.0, 25.0
+    bound = beta / (1 + math.exp(-beta)) * beta_u
+    a = np.concatenate([rng.uniform(-bound, bound, size=(3, 40)),
+                        rng.normal(size=(3, 40)) * 1e-3,
+                        np.zeros((1, 40))])
+    a[0, :4] = [bound, -bound, 1e-7, -2.5e-5]
+    got = O.quantize_activation_fp8(a, beta, beta_u)
+    r = float(np.float32(448.0) / (np.float32(beta) * np.float32(beta_u)))
+    s_h = float((np.float32(beta) * np.float32(beta_u)) / np.float32(448.0))
+    for i in range(a.shape[0]):
+        for j in range(a.shape[1]):
+            assert got[i, j] == _e4m3_nearest(float(a[i, j]) * r) * s_h, (i, j, a[i, j])
+    # the scale is fixed: the small rows lose almost everything, the zero row stays zero
+    assert np.all(got[6] == 0.0)
+    assert np.abs(got[3:6]).max() < 0.05
+
+
+def _brute_fp8_routed_latent(z, idx, w, wq, gamma, beta, beta_u, eps):
+    """Per-token, per-element loops for the fp8 routed experts: z quantized per token (scale
+    absmax / 448 in fp32), expert weights as (q, s) pairs, h with the fixed scale, RMSNorm of
+    each expert row, weighted sum in k order.  Only the table search above rounds to e4m3."""
+    bt, latent = z.shape
+    f32 = np.float32
+    r = float(f32(448.0) / (f32(beta) * f32(beta_u)))
+    s_h = float((f32(beta) * f32(beta_u)) / f32(448.0))
+    out = np.zeros((bt, latent))
+    for t in range(bt):
+        amax = max(abs(float(f32(v))) for v in z[t])
+        s = float(f32(amax) / f32(448.0)) if amax > 0 else 1.0
+        inv = float(f32(1.0) / f32(s))
+        zd = [_e4m3_nearest(float(f32(f32(v) * f32(inv)))) * s for v in z[t]]
+        for k in range(idx.shape[1]):
+            e = int(idx[t, k])
+            (gq, gs), (uq, us), (dq, ds) = wq[e]
+            g = [sum(gq[i][c] * float(gs[i]) * zd[c] for c in range(latent)) for i in range(len(gq))]
+            u = [sum(uq[i][c] * float(us[i]) * zd[c] for c in range(latent)) for i in range(len(uq))]
+            h = []
+            for gi, ui in zip(g, u):
+                gp = beta * math.tanh(gi / beta)
+                a = gp / (1 + math.exp(-gp)) * beta_u * math.tanh(ui / beta_u)
+                h.append(_e4m3_nearest(a * r) * s_h)
+            y = [sum(dq[o][i] * float(ds[o]) * h[i] for i in range(len(h))) for o in range(latent)]
+            rms = math.sqrt(sum(v * v for v in y) / latent + eps)
+            for o in range(latent):
+                out[t, o] += float(w[t, k]) * float(gamma[o]) * y[o] / rms
+    return out
+
+
+def test_fp8_routed_latent_matches_brute_force():
+    """routed_latent_fp8 against the per-element loops above (e4m3 by table search, no shared
+    code with the oracle's rounding).  The gate/up inputs are scaled so that activations reach
+    well into the e4m3 range: an unquantized h, or h with a per-token scale, moves the result
+    by far more than the 1e-12 allowed here."""
+    rng = np.random.default_rng(23)
+    bt, latent, inter, E, K = 4, 8, 6, 3, 2
+    z = O.bf16_round((rng.normal(size=(bt, latent)) * 2).astype(np.float32))
+    z[2] = 0.0                                     # an all-zero token row (scale 1)
+    wq = {}
+    for e in range(E):
+        wq[e] = (O.quantize_rows_e4m3(rng.normal(size=(inter, latent)).astype(np.float32) * np.float32(1.5)),
+                 O.quantize_rows_e4m3(rng.normal(size=(inter, latent)).astype(np.float32) * np.float32(3.0)),
+                 O.quantize_rows_e4m3(rng.normal(size=(latent, inter)).astype(np.float32) * np.float32(0.4)))
+    idx = np.array([[0, 2], [1, 0], [2, 1], [0, 1]], np.int32)
+    w = np.array([[0.7, 0.3], [0.5, 0.5], [0.9, 0.1], [0.25, 0.75]])
+    gamma = 1 + 0.1 * rng.normal(size=latent)
+    got = O.routed_latent_fp8(z, idx, w, wq, gamma, 4.0, 25.0, 1e-6)
+    ref = _brute_fp8_routed_latent(z, idx, w, wq, gamma, 4.0, 25.0, 1e-6)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
