@@ -82,6 +82,8 @@ def peaks():
         j = json.load(open(p))
         return dict(hbm=j["hbm_gbs"], tc=j["bf16_tflops"], tc_sustained=j["bf16_tflops_sustained"],
                     source="measured")
+    print("bench.py: MEASURED_PEAKS.json not found; roofline fractions use the fallback peaks "
+          "(6400 GB/s, 1800 / 1400 TFLOP/s) and say so in peak_source", file=sys.stderr, flush=True)
     return dict(hbm=6400.0, tc=1800.0, tc_sustained=1400.0, source="fallback")
 
 
@@ -358,6 +360,96 @@ def run_ffn(args, ws, rank, local):
     return 0
 
 
+def time_forwards(layer, xs, out, steps, warmup, local, ws):
+    """W untimed forwards, then K forwards timed with CUDA events on the launch stream
+    (synchronised and barriered on both sides), with the per-stage record and a clock
+    sample over the timed region.  Returns (local ms, stage ms summed, calls, launches, clocks)."""
+    from sparse_moe_layer_cutoff_b300.lmoe import lmoe_profile, lmoe_profile_read
+
+    stream = torch.cuda.current_stream()
+    for i in range(warmup):
+        layer.forward(xs[i % len(xs)], out)
+    torch.cuda.synchronize()
+    if layer.sync_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    clocks = ClockSampler(local)
+    barrier(ws)
+    torch.cuda.synchronize()
+    lmoe_profile(layer.ctx, True)
+    clocks.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(steps):
+        layer.forward(xs[i % len(xs)], out)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    lmoe_profile(layer.ctx, False)
+    barrier(ws)
+    st, stage_ms, calls, launches = lmoe_profile_read(layer.ctx)
+    status = layer.sync_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    return e0.elapsed_time(e1), stage_ms, calls, launches, clk
+
+
+def routing_stats(layer, xs):
+    """Experts touched (for the algorithmic byte count) and the load range, from the route of
+    each batch."""
+    touched, load_max, load_min = [], [], []
+    for xb in xs:
+        c = layer.route(xb)["counts"]
+        touched.append(int((c > 0).sum().item()))
+        load_max.append(int(c.max().item()))
+        load_min.append(int(c.min().item()))
+    return sum(touched) / len(touched), max(load_max), min(load_min)
+
+
+def layer_fractions(shape, bt, n_touched, step_s, pk, fp8_experts=False):
+    """The layer's achieved TFLOP/s and GB/s and their fractions of the measured bf16 tensor and
+    HBM peaks; `bound` is the roof that binds (the larger of the two ideal times) and `frac`
+    the fraction of that roof."""
+    flops, layer_bytes, _ = algorithmic(shape, bt, n_touched, fp8_experts=fp8_experts)
+    tc_frac = flops / step_s / 1e12 / pk["tc"]
+    hbm_frac = layer_bytes / step_s / 1e9 / pk["hbm"]
+    bound = "tensor" if flops / (pk["tc"] * 1e12) > layer_bytes / (pk["hbm"] * 1e9) else "hbm"
+    return {"tflops": flops / step_s / 1e12, "tc_frac": tc_frac, "gbs": layer_bytes / step_s / 1e9,
+            "hbm_frac": hbm_frac, "bound": bound, "frac": tc_frac if bound == "tensor" else hbm_frac,
+            "algorithmic_flops": flops, "algorithmic_bytes": layer_bytes, "experts_touched": n_touched}
+
+
+def extra_workload(name, weights, steps, warmup, local, ws, device, pk):
+    """One more line of the layer on the bench's weights: the named workload's token batch (its
+    own seed, and for the skewed one the Zipf logit bias and the repeated-token block), timed
+    as the headline is.  Returns a dict for the JSON line."""
+    from sparse_moe_layer_cutoff_b300 import LatentMoE
+    from workloads import make_bias
+
+    w = WORKLOADS[name]
+    s = w.shape
+    layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=make_bias(w, device))
+    xs = [make_x(w, device), make_x(w, device, seed_offset=1)]
+    out = torch.empty((w.bt, s.d), dtype=layer.dtype, device=device)
+    n_touched, lmax, lmin = routing_stats(layer, xs)
+    ms, stage_ms, calls, launches, clk = time_forwards(layer, xs, out, steps, warmup, local, ws)
+    layer.close()
+    del xs, out
+    torch.cuda.empty_cache()
+    step_s = ms / 1e3 / steps
+    fr = layer_fractions(s, w.bt, n_touched, step_s, pk)
+    return {"workload": w.name, "bt": w.bt, "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
+            "tokens_s": w.bt / step_s, "tc_frac": fr["tc_frac"], "hbm_frac": fr["hbm_frac"],
+            "bound": fr["bound"], "frac": fr["frac"], "experts_touched": n_touched,
+            "expert_load": {"max": lmax, "min": lmin, "target": w.bt * s.top_k / s.n_experts},
+            "stage_ms_per_step": {k: v / max(calls, 1) for k, v in stage_ms.items()},
+            "gpu_launches": launches, "clocks": clk,
+            "inputs": "the headline's weights; x drawn with this workload's seed" +
+                      (", Zipf(1.1) logit bias and 25 % identical tokens" if w.zipf_bias else "")}
+
+
+EXTRA_WORKLOADS = ("full_decode_bt64", "full_skewed_bt16384")
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -375,6 +467,8 @@ def main(argv=None):
                     help="tokens per step instead of the workload's (same shape and recipe); a separate line")
     ap.add_argument("--latent-norm", default="expert", choices=["expert", "combined"],
                     help="latent RMSNorm placement; 'combined' (one norm of the weighted sum) is a separate line")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the decode (64 tokens) and skewed (16384 tokens) figures of the default line")
     args = ap.parse_args(argv)
     if args.e2e_steps is None:
         args.e2e_steps = args.steps
@@ -389,7 +483,7 @@ def main(argv=None):
         return rc
 
     from sparse_moe_layer_cutoff_b300 import LatentMoE
-    from sparse_moe_layer_cutoff_b300.lmoe import lmoe_build_info, lmoe_profile, lmoe_profile_read
+    from sparse_moe_layer_cutoff_b300.lmoe import lmoe_build_info
 
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
@@ -415,41 +509,8 @@ def main(argv=None):
     out = torch.empty((w.bt, s.d), dtype=layer.dtype, device=device)
     stream = torch.cuda.current_stream(device)
 
-    # experts touched (for the algorithmic byte count), from the route of each batch
-    touched, load_max, load_min = [], [], []
-    for xb in xs:
-        r = layer.route(xb)
-        c = r["counts"]
-        touched.append(int((c > 0).sum().item()))
-        load_max.append(int(c.max().item()))
-        load_min.append(int(c.min().item()))
-    n_touched = sum(touched) / len(touched)
-
-    for i in range(args.warmup):
-        layer.forward(xs[i % 2], out)
-    torch.cuda.synchronize()
-    if layer.sync_status() != 0:
-        raise RuntimeError("device status set during warm-up")
-
-    clocks = ClockSampler(local)
-    barrier(ws)
-    torch.cuda.synchronize()
-    lmoe_profile(layer.ctx, True)
-    clocks.start()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.steps):
-        layer.forward(xs[i % 2], out)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    clk = clocks.stop()
-    lmoe_profile(layer.ctx, False)
-    barrier(ws)
-    ms_local = e0.elapsed_time(e1)
-    st, stage_ms, calls, launches = lmoe_profile_read(layer.ctx)
-    status = layer.sync_status()
-    if status != 0:
-        raise RuntimeError(f"device status {status} after the timed region")
+    n_touched, load_max, load_min = routing_stats(layer, xs)
+    ms_local, stage_ms, calls, launches, clk = time_forwards(layer, xs, out, args.steps, args.warmup, local, ws)
     ms = max_over_ranks(ms_local, ws, device)
     tokens_all = sum_over_ranks(float(w.bt * args.steps), ws, device)
     value = tokens_all / (ms / 1e3)
@@ -478,11 +539,8 @@ def main(argv=None):
                                                 " burst" if roof["bound"] == "tensor" else "")
                  + (" bf16 x 2 (nominal fp8 / bf16 ratio)" if (roof["bound"] == "tensor" and f8_kernel) else "")})
     step_s = ms / 1e3 / args.steps
-    layer_roof = {"tflops": flops / step_s / 1e12, "tc_frac": flops / step_s / 1e12 / pk["tc"],
-                  "gbs": layer_bytes / step_s / 1e9, "hbm_frac": layer_bytes / step_s / 1e9 / pk["hbm"],
-                  "algorithmic_flops": flops, "algorithmic_bytes": layer_bytes, "experts_touched": n_touched,
-                  "expert_load": {"max": max(load_max), "min": min(load_min),
-                                  "target": w.bt * s.top_k / s.n_experts}}
+    layer_roof = layer_fractions(s, w.bt, n_touched, step_s, pk, fp8_experts=args.fp8_experts)
+    layer_roof["expert_load"] = {"max": load_max, "min": load_min, "target": w.bt * s.top_k / s.n_experts}
 
     # ---- end to end through the C ABI host-buffer call (lmoe_forward_host): every step copies
     # its input from pinned host memory and its output back to pinned host memory.  Wall clock
@@ -516,6 +574,16 @@ def main(argv=None):
                "sample": f"{args.cpu_tokens} tokens spread over the batch, routed among themselves, "
                          f"{t:.1f} s wall; expert weights fetched from HBM and upcast to fp64 inside the timing"}
 
+    extras = {}
+    default_line = (args.workload == DEFAULT_WORKLOAD and args.bt is None and not args.fp8_experts and
+                    args.latent_norm == "expert" and not args.no_extra)
+    if default_line:
+        layer.close()
+        del xs, out, xh, oh
+        torch.cuda.empty_cache()
+        for name in EXTRA_WORKLOADS:
+            extras[name] = extra_workload(name, weights, args.steps, args.warmup, local, ws, device, pk)
+
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
@@ -539,8 +607,12 @@ def main(argv=None):
         if args.latent_norm != "expert":
             line["metric"] += f" [latent norm: {args.latent_norm}]"
             line["config"]["latent_norm"] = args.latent_norm
+        if extras:
+            line["decode_bt64"] = extras["full_decode_bt64"]
+            line["skewed_bt16384"] = extras["full_skewed_bt16384"]
         print(json.dumps(line), flush=True)
-    layer.close()
+    if not default_line:
+        layer.close()
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0

@@ -265,7 +265,11 @@ LMOE_API lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls,
  *   (ceil(bt / 128) * n_experts + 2 * n_experts + 1) * 4 bytes <= 4 MiB
  * (e.g. bt <= 149,000 at n_experts = 896); larger calls return LMOE_ERR_UNSUPPORTED.
  * The first call on a device looks up the array's device address (once per device, with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture.  After a device
+ * reset (a new primary context) the next call looks it up again.
+ * Ids outside [0, n_experts) are a precondition violation that is not reported: such a
+ * pair is counted in no segment, so offsets[n_experts] is below bt*top_k, the tail of perm
+ * past offsets[n_experts] and the inv entries of those pairs are left unwritten.
  * All calls share the array and it keeps the last call's contents: calls that overlap on
  * the GPU (different streams, or different host threads, without ordering) race on it.
  * bt == 0 returns LMOE_OK without launching. */

@@ -92,8 +92,13 @@ extern "C" lmoe_status lmoe_quantize_fp8_rows(const void* w, int64_t rows, int32
       (reinterpret_cast<uintptr_t>(scale) & 3u))
     return LMOE_ERR_INVALID_ARG;
   if (cols % 8) return LMOE_ERR_UNSUPPORTED;
-  const long long blocks = (rows + 7) / 8;
-  const int grid = (int)(blocks < 148LL * 64 ? blocks : 148LL * 64);
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return LMOE_ERR_CUDA;
+  }
+  const long long blocks = (rows + 7) / 8, cap = (long long)sms * 64;   // 64 blocks per SM at most
+  const int grid = (int)(blocks < cap ? blocks : cap);
   lmoe::quantize_rows_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
       static_cast<const lmoe::bf16*>(w), rows, cols, static_cast<uint8_t*>(q), scale);
   return cudaGetLastError() == cudaSuccess ? LMOE_OK : LMOE_ERR_CUDA;

@@ -29,6 +29,7 @@ struct RouteArgs {
   int32_t* perm;            // [bt * K]
   int32_t* inv;             // [bt * K]
   int32_t* user_counts;     // optional [E]
+  int sm_count;             // SMs of the device (grid sizing)
 };
 
 constexpr int kRouteTailLaunches = 5;   // cutoff, top-K, count, scan, scatter

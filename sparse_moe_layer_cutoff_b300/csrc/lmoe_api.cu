@@ -265,6 +265,7 @@ cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, in
   r.block_cnt = ctx->block_cnt; r.counts = ctx->counts; r.offsets = ctx->offsets;
   r.mtile_off = ctx->mtile_off; r.perm = ctx->perm; r.inv = ctx->inv;
   r.user_counts = user_counts;
+  r.sm_count = ctx->sm_count;
   r.momentum = ctx->momentum;
   r.alpha_prev = (ctx->momentum > 0.0 && ctx->state_valid) ? ctx->alpha_state : nullptr;
   r.alpha_state = ctx->momentum > 0.0 ? ctx->alpha_state : nullptr;

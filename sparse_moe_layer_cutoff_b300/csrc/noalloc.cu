@@ -8,6 +8,8 @@
 // outputs, and the only working memory, the per-block expert counts of the counting
 // sort, lives in the fixed device array below, which every GPU that loads this library
 // holds until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/lmoe.h"
@@ -20,10 +22,35 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) int32_t lmoe_noalloc_scratch[kScratchBytes / sizeof(int32_t)];
 
-std::mutex g_mu;
-int32_t* g_scratch[kMaxDevices];   // device address of the array, per device (host stand-in is not it)
+// Per device: the array's device address and the context it was looked up in (a device reset
+// creates a new primary context, whose address and kernel attributes must be set up again).
+struct ScratchEntry {
+  CUcontext ctx;
+  int32_t* ptr;
+};
 
-// Once per device, with that device current: look up the array's device address.
+std::mutex g_mu;
+ScratchEntry g_scratch[kMaxDevices];   // the host-side name of the array is not its device address
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    cudaGetLastError();
+  }
+  CUcontext c = nullptr;
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
+// With the device current: the array's device address, looked up once per device and
+// context (the lookup also makes the runtime create the device's context if needed).
 lmoe_status scratch_for_current_device(int32_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -31,7 +58,9 @@ lmoe_status scratch_for_current_device(int32_t** out) {
     return LMOE_ERR_CUDA;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch[dev]) {
+  ScratchEntry& ent = g_scratch[dev];
+  const CUcontext cur = current_context();
+  if (!ent.ptr || !cur || ent.ctx != cur) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, lmoe_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
@@ -41,9 +70,10 @@ lmoe_status scratch_for_current_device(int32_t** out) {
       cudaGetLastError();
       return LMOE_ERR_CUDA;
     }
-    g_scratch[dev] = static_cast<int32_t*>(p);
+    ent.ptr = static_cast<int32_t*>(p);
+    ent.ctx = current_context();
   }
-  *out = g_scratch[dev];
+  *out = ent.ptr;
   return LMOE_OK;
 }
 

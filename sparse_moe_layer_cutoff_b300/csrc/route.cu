@@ -454,7 +454,8 @@ cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st) {
   const int tk_warps = topk_warps(a.n_experts);
   const size_t tk_smem = topk_smem_bytes(a.n_experts, tk_warps);
   int tk_grid = (a.bt + tk_warps - 1) / tk_warps;
-  if (tk_grid > 148 * 16) tk_grid = 148 * 16;
+  const int tk_cap = (a.sm_count > 0 ? a.sm_count : 1) * 16;   // 16 blocks per SM at most
+  if (tk_grid > tk_cap) tk_grid = tk_cap;
   topk_kernel<<<tk_grid, tk_warps * 32, tk_smem, st>>>(a.logits, a.alpha, a.bt, a.n_experts,
                                                       a.top_k, a.idx, a.w);
   const int nblk = (a.bt + kSegTokens - 1) / kSegTokens;

@@ -57,3 +57,15 @@ def test_fp8_experts_byte_model():
     assert b16 - b8 == expert_params - scales
     g = st8["expert_gate_up_gemm"][1]
     assert g == 896 * 2 * 3072 * (3584 + 4) + 8192 * 16 * (3584 + 4) + 8192 * 16 * 3072
+
+
+def test_layer_fraction_takes_the_binding_roof():
+    """The layer line's `bound` is the roof with the larger ideal time and `frac` its fraction:
+    at 8192 tokens the 59.8 GB of weights and rows bind (HBM), at 16384 the 23.5 TFLOP do."""
+    pk = {"hbm": 6500.0, "tc": 1756.5}
+    r = bench.layer_fractions(FULL, 8192, 896, 0.0154, pk)
+    assert r["bound"] == "hbm" and r["frac"] == r["hbm_frac"]
+    assert r["hbm_frac"] == pytest.approx(59.80e9 / 0.0154 / 6500e9, rel=1e-3)
+    assert r["tc_frac"] == pytest.approx(11.77e12 / 0.0154 / 1756.5e12, rel=1e-3)
+    r = bench.layer_fractions(FULL, 16384, 896, 0.030, pk)
+    assert r["bound"] == "tensor" and r["frac"] == r["tc_frac"]

@@ -150,13 +150,18 @@ def make_inputs(w: Workload, device="cpu", bt: int | None = None):
             weights[name] = g.to(dt)
             continue
         weights[name] = _randn(shp, _std(name, s), gen, device, dt)
-    bias = None
-    if w.zipf_bias:
-        cg = torch.Generator(device="cpu")
-        cg.manual_seed(w.seed)
-        r = torch.randperm(s.n_experts, generator=cg).to(torch.float64) + 1.0
-        bias = (3.0 * r.pow(-1.1)).to(torch.float32).to(device)
-    return x, weights, bias
+    return x, weights, make_bias(w, device)
+
+
+def make_bias(w: Workload, device="cpu"):
+    """The skewed workload's per-expert Zipf(s=1.1) logit bias b_e = 3.0 * r_e^-1.1, r a random
+    permutation of 1..E from a CPU generator seeded with the workload's seed (fp32), or None."""
+    if not w.zipf_bias:
+        return None
+    cg = torch.Generator(device="cpu")
+    cg.manual_seed(w.seed)
+    r = torch.randperm(w.shape.n_experts, generator=cg).to(torch.float64) + 1.0
+    return (3.0 * r.pow(-1.1)).to(torch.float32).to(device)
 
 
 def make_x(w: Workload, device="cpu", bt: int | None = None, seed_offset: int = 0):
