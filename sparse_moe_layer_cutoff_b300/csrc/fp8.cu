@@ -1,12 +1,12 @@
 // fp8 (e4m3) routed experts: row quantization of expert weights (an entry point of the
-// library) and the quantizing gather of the experts' token rows.
+// library) and of the experts' token rows.
 //
 // "KimiK3的StableLatentMoE架构解析", ¶"第一": the bounded SiTU-GLU output makes fp8 inference
 // possible.  Quantization used here, per row of R values:
 //   s = absmax / 448 in fp32 (1 for an all-zero row), inv = 1 / s (fp32), q = e4m3(x * inv)
 // with e4m3 rounding to nearest, ties to even, saturating at +-448; the row is read back as
 // q * s.  Expert weights are quantized once per output row; the experts' input z once per
-// (token, expert) slot (the same value for all slots of a token).
+// token (the expert GEMM gathers the quantized rows of its tokens).
 #include <cuda_fp8.h>
 
 #include "../../include/lmoe.h"
@@ -61,23 +61,14 @@ __global__ void __launch_bounds__(256) quantize_rows_kernel(const bf16* __restri
     quantize_row_warp(w + r * cols, cols, q + r * cols, scale + r);
 }
 
-// zq[slot] = quantized z[perm[slot]], tscale[slot] = its scale; one warp per slot.
-__global__ void __launch_bounds__(256) gather_quant_kernel(const bf16* __restrict__ z, const int32_t* __restrict__ perm,
-                                                           const int32_t* __restrict__ offsets, int n_experts,
-                                                           int latent, uint8_t* __restrict__ zq,
-                                                           float* __restrict__ tscale) {
-  const int nslots = offsets[n_experts];
-  const int wpb = blockDim.x >> 5;
-  for (int slot = blockIdx.x * wpb + (threadIdx.x >> 5); slot < nslots; slot += gridDim.x * wpb)
-    quantize_row_warp(z + (long long)perm[slot] * latent, latent, zq + (long long)slot * latent, tscale + slot);
-}
-
 }  // namespace
 
-cudaError_t launch_gather_quant(const void* z, const int32_t* perm, const int32_t* offsets, int n_experts, int latent,
-                                void* zq, float* tscale, int grid, cudaStream_t st) {
-  gather_quant_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(z), perm, offsets, n_experts, latent,
-                                            static_cast<uint8_t*>(zq), tscale);
+cudaError_t launch_quantize_rows(const void* x, long long rows, int cols, void* q, float* scale, int grid,
+                                 cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  if (blocks < grid) grid = (int)blocks;
+  quantize_rows_kernel<<<grid, 256, 0, st>>>(static_cast<const bf16*>(x), rows, cols, static_cast<uint8_t*>(q), scale);
   return cudaGetLastError();
 }
 

@@ -9,19 +9,20 @@ namespace lmoe {
 struct TcPlan;  // tensor maps of the borrowed weights and of the workspace, launch shapes
 
 struct TcBuffers {
-  void* z;
-  void* zp;          // [max_bt * K, latent] routed token rows in slot order
+  void* z;           // [max_bt, latent] bf16: the routed experts gather their token rows from it
+  void* zq;          // [max_bt, latent] e4m3 copy of z (fp8 experts only)
+  void* zp;          // [max_bt * K, latent] routed token rows in slot order (bf16, or e4m3 bytes)
   void* h;
   void* y;
   void* cat;
-  float* tscale;     // [max_bt * K] per-slot token scales (fp8 experts)
+  float* tscale;     // [max_bt] per-token scales of zq (fp8 experts)
   uint32_t* status;
 };
 
 // Builds the weight / workspace descriptors.  *plan == nullptr with LMOE_OK means the
 // engine does not cover this configuration.
-// f8 != nullptr: routed experts in e4m3 (w's expert pointers are not used); zp and h then
-// hold e4m3 bytes.
+// f8 != nullptr: routed experts in e4m3 (w's expert pointers are not used); h then holds
+// e4m3 bytes.
 lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int max_bt,
                            int sm_count, const TcBuffers& buf, TcPlan** plan);
 void tc_plan_destroy(TcPlan* plan);
@@ -30,7 +31,7 @@ void tc_plan_destroy(TcPlan* plan);
 // returns.
 void tc_inject_wait_timeout(TcPlan* plan);
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
-int tc_launches(int op);   // kernels launch_gemm_tc starts for one GemmOp
+int tc_launches(int op, bool f8);   // kernels launch_gemm_tc starts for one GemmOp
 
 // Dense SiTU-GLU FFN (out = W_down act(W_gate x, W_up x)) on the same engine: descriptors of
 // the borrowed weights and of the caller-provided h [max_bt, inter] buffer.

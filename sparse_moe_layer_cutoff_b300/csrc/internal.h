@@ -68,6 +68,7 @@ struct GemmArgs {
   const int32_t* seg_off;        // [G + 1] or nullptr
   const int32_t* mtile_off;      // [G + 1] or nullptr
   int G;
+  int bt_tokens;                 // grouped: tokens of the call (rows of A before the gather)
   int max_mtiles;                // launch bound on m-tiles (grouped)
   int epi;
   void* out; long long ldo;      // Store / Glu: T; Router: fp32
@@ -79,9 +80,9 @@ struct GemmArgs {
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, bool is_bf16, cudaStream_t st);
 
-// fp8 experts: zq[slot] = e4m3 rows of z[perm[slot]] with per-slot scales (csrc/fp8.cu).
-cudaError_t launch_gather_quant(const void* z, const int32_t* perm, const int32_t* offsets, int n_experts, int latent,
-                                void* zq, float* tscale, int grid, cudaStream_t st);
+// fp8 experts: q[r] = e4m3 row r of the bf16 rows x [rows, cols] with its scale (csrc/fp8.cu).
+cudaError_t launch_quantize_rows(const void* x, long long rows, int cols, void* q, float* scale, int grid,
+                                 cudaStream_t st);
 
 // ---------------------------------------------------------------------------- checks
 // Sets kStatusAssert in *status unless idx / counts / offsets / perm / inv form valid

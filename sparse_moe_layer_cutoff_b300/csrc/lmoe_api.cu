@@ -29,6 +29,7 @@ struct lmoe_ctx {
   size_t esz;
   bool check;
   bool use_tc;
+  bool f8;              // e4m3 routed experts
   int last_bt;
   double momentum;      // streaming cutoffs: weight of the previous call's cutoff (0 = per call)
   bool state_valid;     // a call has stored its cutoff since momentum was set
@@ -49,7 +50,8 @@ struct lmoe_ctx {
   int32_t* perm;
   int32_t* inv;
   void* z;
-  void* zp;
+  void* zq;             // fp8 experts: e4m3 rows of z
+  void* zp;             // routed token rows in slot order
   void* h;
   void* y;
   void* cat;
@@ -229,7 +231,7 @@ lmoe_status finish(lmoe_ctx* ctx, cudaStream_t st, cudaError_t e) {
 }
 
 cudaError_t run_gemm(lmoe_ctx* ctx, const GemmArgs& g, cudaStream_t st) {
-  ctx->launches += ctx->use_tc ? tc_launches(g.op) : 1;
+  ctx->launches += ctx->use_tc ? tc_launches(g.op, ctx->f8) : 1;
   if (ctx->use_tc) return launch_gemm_tc(ctx->tc, g, st);
   return launch_gemm_simt(g, ctx->bf16, st);
 }
@@ -357,6 +359,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->max_bt = max_bt;
   ctx->stream = static_cast<cudaStream_t>(stream);
   ctx->bf16 = cfg->dtype == LMOE_BF16;
+  ctx->f8 = f8 != nullptr;
   ctx->esz = ctx->bf16 ? 2 : 4;
   const char* chk = getenv("LMOE_CHECK");
   ctx->check = chk && chk[0] == '1';
@@ -387,11 +390,12 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   size_t o_inv = cv.take<int32_t>(bt * K);
   size_t o_status = cv.take<uint32_t>(4);
   size_t o_z = cv.take<char>(bt * L * ctx->esz);
-  size_t o_zp = ctx->bf16 ? cv.take<char>(bt * K * L * ctx->esz) : 0;
+  size_t o_zq = f8 ? cv.take<char>(bt * L) : 0;
+  size_t o_zp = ctx->bf16 ? cv.take<char>(bt * K * L * 2) : 0;
   size_t o_h = cv.take<char>(bt * K * c.expert_inter * ctx->esz);
   size_t o_y = cv.take<char>(bt * K * L * ctx->esz);
   size_t o_cat = cv.take<char>(bt * ldc * ctx->esz);
-  size_t o_tscale = cv.take<float>(bt * K);
+  size_t o_tscale = cv.take<float>(bt);
   ctx->ws_bytes = cv.off;
   if (ws_malloc(reinterpret_cast<void**>(&ctx->ws), ctx->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -413,6 +417,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->inv = (int32_t*)(b + o_inv);
   ctx->status = (uint32_t*)(b + o_status);
   ctx->z = b + o_z;
+  ctx->zq = f8 ? b + o_zq : nullptr;
   ctx->zp = ctx->bf16 ? b + o_zp : nullptr;
   ctx->h = b + o_h;
   ctx->y = b + o_y;
@@ -435,7 +440,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
     }
     if (!(force && force[0] == '1')) {
       TcBuffers tb;
-      tb.z = ctx->z; tb.zp = ctx->zp; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
+      tb.z = ctx->z; tb.zq = ctx->zq; tb.zp = ctx->zp; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
       tb.tscale = ctx->tscale;
       tb.status = ctx->status;
       lmoe_status ts = tc_plan_create(&c, w, f8, max_bt, ctx->sm_count, tb, &ctx->tc);
@@ -538,6 +543,7 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     g.seg_k0[1] = c.latent; g.seg_B[0] = ctx->w.exp_gate; g.seg_ldb[0] = c.latent;
     g.B_up = ctx->w.exp_up; g.b_group_rows = c.expert_inter;
     g.seg_off = ctx->offsets; g.mtile_off = ctx->mtile_off; g.G = c.n_experts; g.max_mtiles = max_mtiles;
+    g.bt_tokens = bt;
     g.epi = kEpiGlu; g.out = ctx->h; g.ldo = c.expert_inter;
     g.op = kOpExpertGateUp;
     e = run_gemm(ctx, g, st);
