@@ -117,9 +117,13 @@ qb_cutoff_kernel(const float* __restrict__ logits_t, int bt, int n_experts, int 
 //   3. Any expert with k32 < v - 2 kKeyTol has an fp64 key below the K-th largest fp64 key
 //      (K experts have fp64 keys >= v - kKeyTol), so it cannot be chosen: the candidates
 //      are the experts with k32 >= v - 2 kKeyTol (usually K or K+1 of them).
-//   4. fp64 keys for the candidates only; each candidate's rank among them (key
-//      descending, ties to the lower expert index) is its output slot if below K.  With
-//      more than 32 candidates (near-ties, K > 32) K rounds of warp argmax do the same.
+//   4. Each candidate's rank among the candidates (key descending, ties to the lower expert
+//      index) is its output slot if below K.  Two candidates whose fp32 keys differ by more
+//      than 2 kKeyTol compare in fp32 (their fp64 keys are in the same order); closer pairs
+//      compare their fp64 keys, which are computed only for candidates with such a
+//      neighbour (on this GPU's narrow fp64 pipe the fp64 sigmoid dominated the kernel).
+//      With more than 32 candidates (near-ties, K > 32) K rounds of warp argmax over fp64
+//      keys do the same.
 // Combine weights are the chosen fp64 scores over their sum (summed in k order).
 // ------------------------------------------------------------------------------------
 constexpr float kKeyTol = 1e-6f;
@@ -215,20 +219,34 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
       nc += __popc(m);
     }
     __syncwarp();
-    for (int j = lane; j < nc; j += 32) {
-      const int e = cid[j];
-      ckey[j] = sigmoid_f64((double)lrow[e]) - s_alpha[e];
-    }
-    __syncwarp();
     // 4. exact selection among the candidates
     if (nc <= 32) {
+      // Two candidates whose fp32 keys differ by more than 2 kKeyTol have their fp64 keys in the
+      // same order; only candidates with a neighbour closer than that need their fp64 key, and
+      // the fp64 evaluation is skipped when no candidate of the token needs it.
+      const int ej = lane < nc ? cid[lane] : 0;
+      const float kj32 = lane < nc ? key_to_f32(ku[ej]) : 0.f;
+      bool near = false;
+      if (lane < nc)
+        for (int i = 0; i < nc; ++i)
+          if (i != lane && fabsf(key_to_f32(ku[cid[i]]) - kj32) <= 2.0f * kKeyTol) near = true;
+      if (__any_sync(0xffffffffu, near)) {
+        if (near) ckey[lane] = sigmoid_f64((double)lrow[ej]) - s_alpha[ej];
+        __syncwarp();
+      }
       if (lane < nc) {
-        const double kj = ckey[lane];
-        const int ej = cid[lane];
         int rank = 0;
         for (int i = 0; i < nc; ++i) {
-          const double ki = ckey[i];
-          rank += (ki > kj || (ki == kj && cid[i] < ej)) ? 1 : 0;
+          const int ei = cid[i];
+          const float ki32 = key_to_f32(ku[ei]);
+          bool beats;
+          if (fabsf(ki32 - kj32) > 2.0f * kKeyTol) {
+            beats = ki32 > kj32;
+          } else {
+            const double ki = ckey[i], kj = ckey[lane];   // both near: fp64 keys computed above
+            beats = ki > kj || (ki == kj && ei < ej);
+          }
+          rank += (i != lane && beats) ? 1 : 0;
         }
         if (rank < top_k) {
           idx_out[(size_t)t * top_k + rank] = ej;
@@ -236,6 +254,11 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
         }
       }
     } else {
+      for (int j = lane; j < nc; j += 32) {
+        const int e = cid[j];
+        ckey[j] = sigmoid_f64((double)lrow[e]) - s_alpha[e];
+      }
+      __syncwarp();
       bool bv = false;
       double bk = 0.0;
       int be = 0;

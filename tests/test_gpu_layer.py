@@ -176,18 +176,55 @@ def test_full_decode_bt64():
     r.check_output(rows=_sample_rows(r.bt), ref_route=ref)
 
 
+def _check_expert_slots(r, ref, slots, tol=2e-2):
+    """The routed experts' stages slot by slot: h[slot] against the oracle's SiTU-GLU of the
+    stored z row of the slot's token, y[slot] against the oracle's down projection of that
+    activation (one expert per slot; each expert's weights are fetched and upcast once)."""
+    s = r.shape
+    off = ref["offsets"]
+    slots = np.asarray(sorted(set(int(v) for v in slots)))
+    experts = np.searchsorted(off, slots, side="right") - 1
+    sl = torch.as_tensor(slots, device="cuda")
+    h = to64(r.ws["h"][sl])
+    y = to64(r.ws["y"][sl])
+    toks = ref["perm"][slots]
+    z = to64(r.ws["z"][torch.as_tensor(toks, device="cuda")])
+    W = oracle_weights(r.weights)
+    worst_h = worst_y = 0.0
+    for e in np.unique(experts):
+        sel = np.nonzero(experts == e)[0]
+        a = O.situ_glu(z[sel] @ W["exp_gate"][e].T, z[sel] @ W["exp_up"][e].T, s.beta, s.beta_u)
+        yr = a @ W["exp_down"][e].T
+        for j, i in enumerate(sel):
+            worst_h = max(worst_h, rel_l2(h[i], a[j]))
+            worst_y = max(worst_y, rel_l2(y[i], yr[j]))
+    assert worst_h < tol and worst_y < tol, (worst_h, worst_y)
+    return len(slots), len(np.unique(experts))
+
+
 @pytest.mark.slow
 def test_full_prefill_bt8192():
+    """Full shape, 8192 tokens: routing in full, the output on sampled rows, and the expert
+    stages on the first and the last slot of every expert segment (the last slot sits in the
+    segment's last token tile, the one narrowed to its token count)."""
     r = Run(WORKLOADS["full_prefill_bt8192"])
     assert r.status == 0
     ref = r.check_routing()
     r.check_logits(rows=[0, 4097, 8191])
     r.check_output(rows=_sample_rows(r.bt), ref_route=ref)
+    off = ref["offsets"]
+    E = r.shape.n_experts
+    slots = [off[e] for e in range(E) if off[e + 1] > off[e]] + [off[e + 1] - 1 for e in range(E) if off[e + 1] > off[e]]
+    n, ne = _check_expert_slots(r, ref, slots)
+    assert ne == E and n == 2 * E
     r.close()
 
 
 @pytest.mark.slow
 def test_full_skewed_bt16384():
+    """Full shape, 16384 tokens with the Zipf logit bias and 25 % identical tokens: routing in
+    full, sampled output rows, and the expert stages of the heavily loaded experts across
+    their token tiles (first and last slot of each tile, and slots inside)."""
     r = Run(WORKLOADS["full_skewed_bt16384"])
     assert r.status == 0
     ref = r.check_routing()
@@ -196,6 +233,19 @@ def test_full_skewed_bt16384():
     r.check_output(rows=_sample_rows(r.bt, extra=(100, 5000)), ref_route=ref)
     nrep = r.bt // 4
     assert torch.equal(r.out[:nrep], r.out[:1].expand(nrep, -1))
+    off = ref["offsets"]
+    heavy = np.nonzero(counts >= 1024)[0]
+    assert len(heavy) >= r.shape.top_k
+    rng = np.random.default_rng(7)
+    slots = []
+    for e in heavy:
+        lo, hi = int(off[e]), int(off[e + 1])
+        tile = 192                   # token tile of the grouped GEMMs
+        for b in range(lo, hi, tile):
+            slots += [b, min(b + tile, hi) - 1]
+        slots += rng.integers(lo, hi, size=4).tolist()
+    n, ne = _check_expert_slots(r, ref, slots)
+    assert n >= 64 and ne == len(heavy)
     r.close()
 
 

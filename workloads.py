@@ -76,6 +76,11 @@ WORKLOADS = {
     # profiling case for the token-row kernels (gather, RMSNorm + combine): 2048 tokens x 16
     # expert rows of latent 3584 are 235 MB per pass, above the 126 MB L2, as at bt = 8192
     "profile_e32_bt2048": Workload("profile_e32_bt2048", dataclasses.replace(FULL, n_experts=32), 2048, 6),
+    # profiling case for every other kernel at its full-size shape: the router (896 experts at
+    # d = 7168), cutoffs, top-K and segments at 8192 tokens, W_down, the shared experts, W_up +
+    # shared down, the gather and the combine; only the routed experts' intermediate size is cut
+    # to 64 (1.6 GB of weights in all), so multi-pass counter captures stay small
+    "profile_layer_bt8192": Workload("profile_layer_bt8192", dataclasses.replace(FULL, expert_inter=64), 8192, 7),
 }
 
 
