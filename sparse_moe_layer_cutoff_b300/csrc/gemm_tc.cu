@@ -42,31 +42,42 @@ namespace {
 
 constexpr int kBK = 64;
 constexpr int kHalf = 128;                       // weight rows per MMA (M)
-constexpr int kTokMax = kTileM;                  // tokens per tile (MMA N), a multiple of 16
+constexpr int kTokMax = kTileM;                  // tokens per tile of the grouped GEMMs (MMA N)
 constexpr int kTokBox = 16;                      // token rows per TMA box
 constexpr int kHalfBytes = kHalf * kBK * 2;      // 16 KB
 constexpr int kWStageBytes = 2 * kHalfBytes;     // 32 KB of weights per stage
-constexpr int kTStageBytes = kTokMax * kBK * 2;  // token rows per stage
 constexpr int kWStages = 4;
 constexpr int kTStages = 3;
 constexpr int kSlotCols = 256;
 constexpr int kEpiWarps = 12;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kThreads = 128 + kEpiThreads;
-constexpr int kMaxChunks = (kTokMax / 32 + 2) / 3;   // 32-token chunks per epilogue warp
+constexpr int kStaged = 2;                       // 32-token chunks an epilogue warp keeps in registers
 constexpr int kSchedMax = 1024;                  // schedule entries kept in shared memory
 constexpr int kDenseGroup = 8;                   // token tiles per raster group (dense GEMMs)
 // barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
 constexpr int kNumBars = 2 * kWStages + 2 * kTStages + 4 + 1;
-constexpr int kOffT = kWStages * kWStageBytes;
-constexpr int kOffSched = kOffT + kTStages * kTStageBytes;
-constexpr int kOffBars = kOffSched + 2 * kSchedMax * 4;
-constexpr int kOffMisc = kOffBars + kNumBars * 8;
-constexpr int kSmemBytes = 1024 + kOffMisc + 16;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
-static_assert(kTokMax % 16 == 0 && kTokMax <= 256, "MMA N limit");
-static_assert(kSmemBytes <= 232448, "shared memory per block");
+
+// Shared-memory layout of the grouped (routed experts) and dense launches.  Dense GEMMs take
+// token tiles of up to 256 (more MMA work per k-block to cover the L2 round trip of their
+// operands) and need no expert schedule; grouped ones keep tiles of kTokMax tokens and the
+// schedule.
+template <bool DENSE>
+struct Geo {
+  static constexpr int kTok = DENSE ? 256 : kTokMax;             // tokens per tile at most
+  static constexpr int kTStageBytes = kTok * kBK * 2;            // token rows per stage
+  static constexpr int kChunks = (kTok / 32 + 2) / 3;           // 32-token chunks per epilogue warp
+  static constexpr int kOffT = kWStages * kWStageBytes;
+  static constexpr int kOffSched = kOffT + kTStages * kTStageBytes;
+  static constexpr int kOffBars = kOffSched + (DENSE ? 0 : 2 * kSchedMax * 4);
+  static constexpr int kOffMisc = kOffBars + kNumBars * 8;
+  static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
+  static_assert(kTok % 16 == 0 && kTok <= 256, "MMA N limit");
+  static_assert(kChunks <= kStaged + 1, "at most one chunk per warp is written before TMEM is released");
+  static_assert(kSmemBytes <= 232448, "shared memory per block");
+};
 
 struct TcMaps {
   CUtensorMap w[kMaxKSeg];  // weight (MMA A) maps, one per K segment; GLU: w[0] = gate
@@ -341,20 +352,21 @@ __device__ __forceinline__ uint32_t acc_col(bool wide, int slot, int h) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int EPI, bool F8 = false>
+template <int EPI, bool F8, bool DENSE>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  using G = Geo<DENSE>;
   constexpr int kBKe = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw);
   const uint32_t wbase = base;
-  const uint32_t tbase = base + kOffT;
-  int32_t* s_seg = reinterpret_cast<int32_t*>(sbase + kOffSched);
+  const uint32_t tbase = base + G::kOffT;
+  int32_t* s_seg = reinterpret_cast<int32_t*>(sbase + G::kOffSched);
   int32_t* s_mt = s_seg + kSchedMax;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + kOffBars);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + kOffMisc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + G::kOffBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + G::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
@@ -374,7 +386,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const bool sched_smem = p.G > 0 && p.G < kSchedMax;
+  const bool sched_smem = !DENSE && p.G > 0 && p.G < kSchedMax;
   if (sched_smem) {
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
       s_seg[i] = p.seg_off[i];
@@ -467,7 +479,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         }
         if (lane == 0) mbar_expect_tx(tfull_bar(stage), (uint32_t)ntr * (kBK * 2));
         __syncwarp();
-        const uint32_t dst = tbase + stage * kTStageBytes;
+        const uint32_t dst = tbase + stage * G::kTStageBytes;
         if (lane < nbox)
           tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, k_rot(p, tl, kb) * kBKe, tl.tok0 + lane * kTokBox,
                       tfull_bar(stage), tpol);
@@ -508,7 +520,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
               !mbar_wait(tfull_bar(ts), tph, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           tc_fence_after();
           const uint64_t ad = smem_desc(wbase + ws * kWStageBytes);
-          const uint64_t bd = smem_desc(tbase + ts * kTStageBytes);
+          const uint64_t bd = smem_desc(tbase + ts * G::kTStageBytes);
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)
             tc_mma_k<F8>(d0, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
@@ -563,9 +575,28 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const uint32_t c0 = lane_base + acc_col(wide, slot, 0);
       const uint32_t c1 = lane_base + acc_col(wide, slot, 1);
       const int nchunks = (tl.ntok + 31) >> 5;
-      // Results of this warp's chunks (<= kMaxChunks), packed bf16 pairs of consecutive
-      // tokens; TMEM is released before they are written out.
-      uint32_t res[kMaxChunks][2][16];
+      const int fbase = EPI == kEpiGlu ? tl.fb * kHalf + q * 32 + lane : tl.fb * 2 * kHalf + q * 32 + lane;
+      // Writes one packed 32-token chunk of output half h (bf16 pairs of consecutive tokens,
+      // or e4m3 quads for the fp8 GLU) to its rows.
+      auto store_chunk = [&](int c, int h, const uint32_t* w) {
+        const int nj = min(32, tl.ntok - c * 32);
+        const int fout = fbase + h * kHalf;
+        if (fout >= p.n_feat) return;
+        if (F8 && EPI == kEpiGlu) {
+          uint8_t* o = static_cast<uint8_t*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nj) o[(long long)j * p.ldo] = (uint8_t)(w[j >> 2] >> (8 * (j & 3)));
+        } else {
+          bf16* o = static_cast<bf16*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < nj) o[(long long)j * p.ldo] = __ushort_as_bfloat16((unsigned short)((j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu)));
+        }
+      };
+      // Results of this warp's first kStaged chunks stay in registers and are written after
+      // TMEM is released; later chunks (tiles of more than 192 tokens) are written at once.
+      uint32_t res[kStaged][2][16];
       if (EPI == kEpiGlu) {
         // fp8: per-row weight scales of this lane's feature (gate and up rows)
         float sg = 1.f, su = 1.f;
@@ -577,10 +608,10 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           }
         }
 #pragma unroll
-        for (int ci = 0; ci < kMaxChunks; ++ci) {
+        for (int ci = 0; ci < G::kChunks; ++ci) {
           const int c = sub + 3 * ci;
           if (c < nchunks) {
-            uint32_t g[32], u[32];
+            uint32_t g[32], u[32], w[16];
             tmem_ld32(c0 + c * 32, g);
             tmem_ld32(c1 + c * 32, u);
             float ts = 1.f;   // fp8: this lane's token scale (lane j holds token j of the chunk)
@@ -597,25 +628,31 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                                                 __uint_as_float(u[j + b]) * (su * tj), p);
                   word |= (uint32_t)e4m3_byte(a * p.h_mul) << (8 * b);
                 }
-                res[ci][0][j >> 2] = word;
+                w[j >> 2] = word;
               }
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
-                res[ci][0][j] = pack_bf16x2(situ_glu_fast(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]), p),
-                                            situ_glu_fast(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]), p));
+                w[j] = pack_bf16x2(situ_glu_fast(__uint_as_float(g[2 * j]), __uint_as_float(u[2 * j]), p),
+                                   situ_glu_fast(__uint_as_float(g[2 * j + 1]), __uint_as_float(u[2 * j + 1]), p));
+            }
+            if (ci < kStaged) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) res[ci < kStaged ? ci : 0][0][j] = w[j];
+            } else {
+              store_chunk(c, 0, w);
             }
           }
         }
       } else if (EPI == kEpiStore) {
 #pragma unroll
-        for (int ci = 0; ci < kMaxChunks; ++ci) {
+        for (int ci = 0; ci < G::kChunks; ++ci) {
           const int c = sub + 3 * ci;
           if (c < nchunks) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               if (h < nh) {
-                uint32_t v[32];
+                uint32_t v[32], w[16];
                 tmem_ld32((h ? c1 : c0) + c * 32, v);
                 float sc = 1.f;   // fp8: row scale times the activation scale
                 if (F8) {
@@ -625,7 +662,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
-                  res[ci][h][j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sc, __uint_as_float(v[2 * j + 1]) * sc);
+                  w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * sc, __uint_as_float(v[2 * j + 1]) * sc);
+                if (ci < kStaged) {
+#pragma unroll
+                  for (int j = 0; j < 16; ++j) res[ci < kStaged ? ci : 0][h][j] = w[j];
+                } else {
+                  store_chunk(c, h, w);
+                }
               }
             }
           }
@@ -670,31 +713,13 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         else mbar_arrive(aempty_bar(slot));
       }
       if (EPI != kEpiRouter) {
-        const int fbase = EPI == kEpiGlu ? tl.fb * kHalf + q * 32 + lane : tl.fb * 2 * kHalf + q * 32 + lane;
 #pragma unroll
-        for (int ci = 0; ci < kMaxChunks; ++ci) {
+        for (int ci = 0; ci < kStaged; ++ci) {
           const int c = sub + 3 * ci;
           if (c >= nchunks) continue;
-          const int nj = min(32, tl.ntok - c * 32);
 #pragma unroll
-          for (int h = 0; h < (EPI == kEpiGlu ? 1 : 2); ++h) {
-            const int fout = fbase + h * kHalf;
-            if (h >= nh || fout >= p.n_feat) continue;
-            if (F8 && EPI == kEpiGlu) {
-              uint8_t* o = static_cast<uint8_t*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nj) o[(long long)j * p.ldo] = (uint8_t)(res[ci][0][j >> 2] >> (8 * (j & 3)));
-            } else {
-              bf16* o = static_cast<bf16*>(p.out) + (long long)(tl.tok0 + c * 32) * p.ldo + fout;
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (j < nj) {
-                  const uint32_t w2 = res[ci][h][j >> 1];
-                  o[(long long)j * p.ldo] = __ushort_as_bfloat16((unsigned short)((j & 1) ? (w2 >> 16) : (w2 & 0xffffu)));
-                }
-            }
-          }
+          for (int h = 0; h < (EPI == kEpiGlu ? 1 : 2); ++h)
+            if (h < nh) store_chunk(c, h, res[ci][h]);
         }
       }
       if (wide) { aph[0] ^= 1u; aph[1] ^= 1u; }
@@ -759,20 +784,27 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Token tile of a dense GEMM: the multiple of 16 in [128, kTokMax] that minimises
+// Token tile of a dense GEMM: the multiple of 16 in [128, 256] that minimises
 // waves x (tile + a fixed per-tile cost of 32 tokens), so the last wave of the persistent
 // grid is nearly full (e.g. the 8192-token router: 172 tiles of 192 tokens leave most of
 // the second wave idle; 256 tiles of 128 fill it, and narrow tiles double-buffer TMEM).
 int dense_tok_tile(int bt, int n_fb, int grid) {
-  int best = kTokMax;
+  constexpr int kMax = Geo<true>::kTok;
+  int best = kMax;
   long long best_cost = -1;
-  for (int tt = kTokMax; tt >= 128; tt -= 16) {
+  for (int tt = kMax; tt >= 128; tt -= 16) {
     const long long tiles = (long long)((bt + tt - 1) / tt) * n_fb;
     const long long waves = (tiles + grid - 1) / grid;
     const long long cost = waves * (tt + 32);
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = tt; }
   }
   return best;
+}
+
+template <int EPI, bool F8, bool DENSE>
+cudaError_t launch_kernel(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t st) {
+  tc_gemm_kernel<EPI, F8, DENSE><<<grid, kThreads, Geo<DENSE>::kSmemBytes, st>>>(maps, p);
+  return cudaGetLastError();
 }
 
 // One launch of the persistent kernel: grid = SMs (fewer when a dense GEMM has fewer tiles).
@@ -784,17 +816,37 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
     if (tiles < grid) grid = (int)tiles;
   }
   if (grid <= 0) return cudaSuccess;
-  if (f8) {
-    if (epi == kEpiGlu) tc_gemm_kernel<kEpiGlu, true><<<grid, kThreads, kSmemBytes, st>>>(maps, p);
-    else tc_gemm_kernel<kEpiStore, true><<<grid, kThreads, kSmemBytes, st>>>(maps, p);
-    return cudaGetLastError();
+  if (f8) {   // the fp8 routed experts (grouped)
+    if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false>(maps, p, grid, st);
+    return launch_kernel<kEpiStore, true, false>(maps, p, grid, st);
+  }
+  if (p.G > 0) {
+    if (epi == kEpiGlu) return launch_kernel<kEpiGlu, false, false>(maps, p, grid, st);
+    return launch_kernel<kEpiStore, false, false>(maps, p, grid, st);
   }
   switch (epi) {
-    case kEpiStore: tc_gemm_kernel<kEpiStore><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
-    case kEpiGlu: tc_gemm_kernel<kEpiGlu><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
-    default: tc_gemm_kernel<kEpiRouter><<<grid, kThreads, kSmemBytes, st>>>(maps, p); break;
+    case kEpiStore: return launch_kernel<kEpiStore, false, true>(maps, p, grid, st);
+    case kEpiGlu: return launch_kernel<kEpiGlu, false, true>(maps, p, grid, st);
+    default: return launch_kernel<kEpiRouter, false, true>(maps, p, grid, st);
   }
-  return cudaGetLastError();
+}
+
+template <int EPI, bool F8, bool DENSE>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Geo<DENSE>::kSmemBytes);
+}
+
+// Raises the dynamic shared-memory limit of every kernel instance a plan launches.
+cudaError_t prepare_kernels(bool f8) {
+  cudaError_t e = set_smem<kEpiStore, false, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiGlu, false, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiRouter, false, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiStore, false, false>();
+  if (e == cudaSuccess) e = set_smem<kEpiGlu, false, false>();
+  if (e == cudaSuccess && f8) e = set_smem<kEpiGlu, true, false>();
+  if (e == cudaSuccess && f8) e = set_smem<kEpiStore, true, false>();
+  return e;
 }
 
 }  // namespace
@@ -852,15 +904,7 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const 
     delete pl;
     return LMOE_ERR_CUDA;
   }
-  cudaError_t e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiStore>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiRouter>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess && pl->f8)
-    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess && pl->f8)
-    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiStore, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = prepare_kernels(pl->f8);
   if (e != cudaSuccess) {
     cudaGetLastError();
     delete pl;
@@ -895,7 +939,6 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   p.inv_beta_u = 1.0f / a.beta_u;
   p.status = pl->buf.status;
   p.timeout_ns = kTimeoutNs;
-  p.tok_tile = kTokMax;
   int epi = a.epi;
   bool ok = true, f8 = false;
   switch (a.op) {
@@ -1020,11 +1063,7 @@ lmoe_status tc_ffn_create(int d, int inter, float beta, float beta_u, const void
   const bool ok = make_map(&pl->m_gate, w_gate, inter, d, d, kHalf) && make_map(&pl->m_up, w_up, inter, d, d, kHalf) &&
                   make_map(&pl->m_down, w_down, d, inter, inter, kHalf) &&
                   make_map(&pl->m_h, h, max_bt, inter, inter, kTokBox);
-  cudaError_t e = ok ? cudaFuncSetAttribute(tc_gemm_kernel<kEpiStore>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kSmemBytes)
-                     : cudaErrorInvalidValue;
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(tc_gemm_kernel<kEpiGlu>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = ok ? prepare_kernels(false) : cudaErrorInvalidValue;
   if (e != cudaSuccess) {
     cudaGetLastError();
     delete pl;
