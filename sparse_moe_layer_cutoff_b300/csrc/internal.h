@@ -30,9 +30,11 @@ struct RouteArgs {
   int32_t* inv;             // [bt * K]
   int32_t* user_counts;     // optional [E]
   int sm_count;             // SMs of the device (grid sizing)
+  int32_t* list;            // [bt] tokens the fast top-K kernel leaves to the general one
+  int32_t* list_count;      // [1]
 };
 
-constexpr int kRouteTailLaunches = 5;   // cutoff, top-K, count, scan, scatter
+constexpr int kRouteTailLaunches = 6;   // cutoff, top-K (fast, general), count, scan, scatter
 cudaError_t route_tail_prepare();
 cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st);
 // Only the segmentation chain (count, scan, scatter) on caller-supplied buffers.

@@ -49,6 +49,7 @@ struct lmoe_ctx {
   int32_t* mtile_off;
   int32_t* perm;
   int32_t* inv;
+  int32_t* topk_list;   // [max_bt + 1] tokens left to the general top-K kernel, then their count
   void* z;
   void* zq;             // fp8 experts: e4m3 rows of z
   void* zp;             // routed token rows in slot order
@@ -268,6 +269,8 @@ cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, in
   r.mtile_off = ctx->mtile_off; r.perm = ctx->perm; r.inv = ctx->inv;
   r.user_counts = user_counts;
   r.sm_count = ctx->sm_count;
+  r.list = ctx->topk_list;
+  r.list_count = ctx->topk_list + ctx->max_bt;
   r.momentum = ctx->momentum;
   r.alpha_prev = (ctx->momentum > 0.0 && ctx->state_valid) ? ctx->alpha_state : nullptr;
   r.alpha_state = ctx->momentum > 0.0 ? ctx->alpha_state : nullptr;
@@ -388,6 +391,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   size_t o_mt = cv.take<int32_t>(E + 1);
   size_t o_perm = cv.take<int32_t>(bt * K);
   size_t o_inv = cv.take<int32_t>(bt * K);
+  size_t o_list = cv.take<int32_t>(bt + 1);
   size_t o_status = cv.take<uint32_t>(4);
   size_t o_z = cv.take<char>(bt * L * ctx->esz);
   size_t o_zq = f8 ? cv.take<char>(bt * L) : 0;
@@ -415,6 +419,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->mtile_off = (int32_t*)(b + o_mt);
   ctx->perm = (int32_t*)(b + o_perm);
   ctx->inv = (int32_t*)(b + o_inv);
+  ctx->topk_list = (int32_t*)(b + o_list);
   ctx->status = (uint32_t*)(b + o_status);
   ctx->z = b + o_z;
   ctx->zq = f8 ? b + o_zq : nullptr;

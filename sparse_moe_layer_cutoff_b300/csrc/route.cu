@@ -22,8 +22,9 @@ constexpr int kCutoffThreads = 256;
 __global__ void __launch_bounds__(kCutoffThreads)
 qb_cutoff_kernel(const float* __restrict__ logits_t, int bt, int n_experts, int top_k,
                  double* __restrict__ alpha, const double* __restrict__ alpha_prev, double momentum,
-                 double* __restrict__ alpha_state) {
+                 double* __restrict__ alpha_state, int32_t* __restrict__ list_count) {
   const int e = blockIdx.x;
+  if (e == 0 && threadIdx.x == 0) *list_count = 0;   // the top-K kernels' list starts empty
   const float* col = logits_t + (size_t)e * bt;
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_bucket, s_below;
@@ -152,7 +153,8 @@ __device__ __forceinline__ void warp_best(bool& v, double& k, int& e) {
 
 __global__ void __launch_bounds__(kTopkMaxWarps * 32)
 topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, int bt,
-            int n_experts, int top_k, int32_t* __restrict__ idx_out, float* __restrict__ w_out) {
+            int n_experts, int top_k, int32_t* __restrict__ idx_out, float* __restrict__ w_out,
+            const int32_t* __restrict__ list, const int32_t* __restrict__ list_count) {
   extern __shared__ double smem_d[];
   const int nwarps = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -163,6 +165,7 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
   float* s_alpha32 = reinterpret_cast<float*>(smem_d + (size_t)(nwarps + 1) * E + (size_t)nwarps * kMaxTopK);
   uint32_t* ku = reinterpret_cast<uint32_t*>(s_alpha32 + E) + (size_t)warp * 2 * E;   // [E] fp32 keys
   int32_t* cid = reinterpret_cast<int32_t*>(ku + E);                              // [E] candidates
+  if (list && *list_count == 0) return;
 
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const double a = alpha[e];
@@ -171,7 +174,10 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
   }
   __syncthreads();
 
-  for (int t = blockIdx.x * nwarps + warp; t < bt; t += gridDim.x * nwarps) {
+  // every token, or only the tokens of the list (those the fast kernel left to this one)
+  const int ntok = list ? *list_count : bt;
+  for (int it = blockIdx.x * nwarps + warp; it < ntok; it += gridDim.x * nwarps) {
+    const int t = list ? list[it] : it;
     const float* lrow = logits + (size_t)t * E;
     // 1. fp32 keys (also kept in registers when every lane has at most kRegKeys of them)
     uint32_t kr[kRegKeys];
@@ -298,6 +304,134 @@ topk_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, 
       w_out[(size_t)t * top_k + k] = (float)(chosen_s[k] / total);
     __syncwarp();
   }
+}
+
+// ------------------------------------------------------------------------------------
+// Top-K, fast path (E <= 32 * kRegKeys, K <= 32): one warp per token with the token's fp32
+// keys in registers.  A float threshold t with at least K keys >= t and at most 32 keys >=
+// t - 2 kKeyTol is found by bisection (keys lie in (-1, 1); the K-th key usually sits near 0,
+// where the cutoffs put about K of the E keys above zero).  Every expert below t - 2 kKeyTol
+// then has an fp64 key below those of the >= K experts at or above t, so the selection lies
+// among the <= 32 candidates, which are ranked exactly as in topk_kernel (fp64 keys only for
+// candidates with a neighbour closer than 2 kKeyTol).  Tokens with no such threshold (massive
+// ties) are appended to `list` for topk_kernel.  Same outputs as topk_kernel, bit for bit.
+// ------------------------------------------------------------------------------------
+constexpr int kFastWarps = 8;
+
+__global__ void __launch_bounds__(kFastWarps * 32)
+topk_fast_kernel(const float* __restrict__ logits, const double* __restrict__ alpha, int bt, int n_experts,
+                 int top_k, int32_t* __restrict__ idx_out, float* __restrict__ w_out, int32_t* __restrict__ list,
+                 int32_t* __restrict__ list_count) {
+  extern __shared__ double smem_d[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = n_experts;
+  double* s_alpha = smem_d;                                                    // [E]
+  double* ck64 = smem_d + E + warp * 32;                                       // [32] per warp
+  double* chosen_s = smem_d + E + kFastWarps * 32 + warp * 32;                 // [32] per warp
+  float* s_alpha32 = reinterpret_cast<float*>(smem_d + E + kFastWarps * 64);   // [E]
+  float* ck32 = s_alpha32 + E + warp * 32;                                     // [32] per warp
+  int32_t* cid = reinterpret_cast<int32_t*>(s_alpha32 + E + kFastWarps * 32) + warp * 32;  // [32] per warp
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const double a = alpha[e];
+    s_alpha[e] = a;
+    s_alpha32[e] = (float)a;
+  }
+  __syncthreads();
+  const unsigned full = 0xffffffffu;
+  const bool usable = E <= 32 * kRegKeys && top_k <= 32;
+  for (int t = blockIdx.x * kFastWarps + warp; t < bt; t += gridDim.x * kFastWarps) {
+    if (!usable) {
+      if (lane == 0) list[atomicAdd(list_count, 1)] = t;
+      continue;
+    }
+    const float* lrow = logits + (size_t)t * E;
+    float kf[kRegKeys];
+#pragma unroll
+    for (int i = 0; i < kRegKeys; ++i) {
+      const int e = lane + 32 * i;
+      kf[i] = e < E ? 1.0f / (1.0f + expf(-lrow[e])) - s_alpha32[e] : -INFINITY;
+    }
+    auto count_ge = [&](float thr) {
+      uint32_t c = 0;
+#pragma unroll
+      for (int i = 0; i < kRegKeys; ++i) c += kf[i] >= thr ? 1u : 0u;
+      return (int)__reduce_add_sync(full, c);
+    };
+    // threshold: count(>= t) >= K and count(>= t - 2 tol) <= 32
+    float lo = -2.0f, hi = 2.0f, tt = 0.0f;
+    bool found = false;
+    for (int step = 0; step < 48; ++step) {
+      if (count_ge(tt) < top_k) {
+        hi = tt;
+      } else if (count_ge(tt - 2.0f * kKeyTol) <= 32) {
+        found = true;
+        break;
+      } else {
+        lo = tt;
+      }
+      const float mid = 0.5f * (lo + hi);
+      if (mid == lo || mid == hi) break;
+      tt = mid;
+    }
+    if (!found) {
+      if (lane == 0) list[atomicAdd(list_count, 1)] = t;
+      continue;
+    }
+    // candidates, in expert order
+    const float thr = tt - 2.0f * kKeyTol;
+    int nc = 0;
+#pragma unroll
+    for (int i = 0; i < kRegKeys; ++i) {
+      const bool c = kf[i] >= thr;
+      const unsigned m = __ballot_sync(full, c);
+      if (c) {
+        const int pos = nc + __popc(m & ((1u << lane) - 1u));
+        cid[pos] = lane + 32 * i;
+        ck32[pos] = kf[i];
+      }
+      nc += __popc(m);
+    }
+    __syncwarp();
+    // exact ranks: fp32 order for candidates further apart than 2 tol, fp64 keys otherwise
+    const int ej = lane < nc ? cid[lane] : 0;
+    const float kj32 = lane < nc ? ck32[lane] : 0.f;
+    bool near = false;
+    if (lane < nc)
+      for (int i = 0; i < nc; ++i)
+        if (i != lane && fabsf(ck32[i] - kj32) <= 2.0f * kKeyTol) near = true;
+    if (__any_sync(full, near)) {
+      if (near) ck64[lane] = sigmoid_f64((double)lrow[ej]) - s_alpha[ej];
+      __syncwarp();
+    }
+    if (lane < nc) {
+      int rank = 0;
+      for (int i = 0; i < nc; ++i) {
+        const float ki32 = ck32[i];
+        bool beats;
+        if (fabsf(ki32 - kj32) > 2.0f * kKeyTol) {
+          beats = ki32 > kj32;
+        } else {
+          const double ki = ck64[i], kj = ck64[lane];
+          beats = ki > kj || (ki == kj && cid[i] < ej);
+        }
+        rank += (i != lane && beats) ? 1 : 0;
+      }
+      if (rank < top_k) {
+        idx_out[(size_t)t * top_k + rank] = ej;
+        chosen_s[rank] = sigmoid_f64((double)lrow[ej]);
+      }
+    }
+    __syncwarp();
+    // combine weights: chosen raw scores over their sum (summed in k order, fp64)
+    double total = 0.0;
+    for (int k = 0; k < top_k; ++k) total = total + chosen_s[k];
+    if (lane < top_k) w_out[(size_t)t * top_k + lane] = (float)(chosen_s[lane] / total);
+    __syncwarp();
+  }
+}
+
+size_t topk_fast_smem_bytes(int n_experts) {
+  return (size_t)n_experts * (sizeof(double) + sizeof(float)) + (size_t)kFastWarps * 32 * (2 * sizeof(double) + sizeof(float) + sizeof(int32_t));
 }
 
 size_t topk_smem_bytes(int n_experts, int nwarps) {
@@ -473,14 +607,19 @@ seg_scatter_kernel(const int32_t* __restrict__ idx, int bt, int top_k, int n_exp
 cudaError_t launch_route_tail(const RouteArgs& a, cudaStream_t st) {
   if (a.bt <= 0) return cudaSuccess;
   qb_cutoff_kernel<<<a.n_experts, kCutoffThreads, 0, st>>>(a.logits_t, a.bt, a.n_experts, a.top_k, a.alpha,
-                                                          a.alpha_prev, a.momentum, a.alpha_state);
+                                                          a.alpha_prev, a.momentum, a.alpha_state, a.list_count);
+  const int sms = a.sm_count > 0 ? a.sm_count : 1;
+  // fast path for every token it can decide; the exact general kernel for the listed rest
+  int fast_grid = (a.bt + kFastWarps - 1) / kFastWarps;
+  if (fast_grid > sms * 8) fast_grid = sms * 8;
+  topk_fast_kernel<<<fast_grid, kFastWarps * 32, topk_fast_smem_bytes(a.n_experts), st>>>(
+      a.logits, a.alpha, a.bt, a.n_experts, a.top_k, a.idx, a.w, a.list, a.list_count);
   const int tk_warps = topk_warps(a.n_experts);
   const size_t tk_smem = topk_smem_bytes(a.n_experts, tk_warps);
   int tk_grid = (a.bt + tk_warps - 1) / tk_warps;
-  const int tk_cap = (a.sm_count > 0 ? a.sm_count : 1) * 16;   // 16 blocks per SM at most
-  if (tk_grid > tk_cap) tk_grid = tk_cap;
+  if (tk_grid > sms * 2) tk_grid = sms * 2;
   topk_kernel<<<tk_grid, tk_warps * 32, tk_smem, st>>>(a.logits, a.alpha, a.bt, a.n_experts,
-                                                      a.top_k, a.idx, a.w);
+                                                      a.top_k, a.idx, a.w, a.list, a.list_count);
   const int nblk = (a.bt + kSegTokens - 1) / kSegTokens;
   const size_t seg_smem = (size_t)kSegWarps * a.n_experts * sizeof(uint32_t);
   seg_count_kernel<<<nblk, kSegThreads, seg_smem, st>>>(a.idx, a.bt, a.top_k, a.n_experts,
@@ -509,6 +648,9 @@ cudaError_t route_tail_prepare() {
   // dynamic shared memory above 48 KB for the largest supported expert count
   cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)topk_smem_bytes(kMaxExperts, topk_warps(kMaxExperts)));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(topk_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)topk_fast_smem_bytes(kMaxExperts));
   if (e != cudaSuccess) return e;
   const int seg = kSegWarps * kMaxExperts * (int)sizeof(uint32_t);
   e = cudaFuncSetAttribute(seg_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, seg);
