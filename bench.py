@@ -40,8 +40,11 @@ METRIC = "LatentMoE layer fwd tokens/s on 1 B300; % of bf16 TC peak (or HBM BW)"
 def algorithmic(shape, bt, n_touched, fp8_experts=False):
     """Algorithmic FLOPs and bytes of one layer call and of each stage (2*M*N*K per GEMM;
     bytes = what each stage must read and write at least once).  n_touched = experts
-    with at least one token.  With fp8 experts their weights, token rows and activations
-    are one byte per value (plus 4-byte row scales)."""
+    with at least one token.  For the routed-expert GEMMs the bytes are the touched experts'
+    weights only, the per-expert unit of the layer's byte count: their token rows and
+    activations are intermediates of the layer (implementation traffic, which the measured
+    DRAM traffic shows on top).  With fp8 experts the weights are one byte per value plus
+    4-byte row scales."""
     d, L, E, K, I, S, Is = (shape.d, shape.latent, shape.n_experts, shape.top_k, shape.expert_inter,
                             shape.n_shared, shape.shared_inter)
     b = 2 if shape.dtype == "bf16" else 4
@@ -50,9 +53,8 @@ def algorithmic(shape, bt, n_touched, fp8_experts=False):
             "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
             "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
             "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
-            "expert_gate_up_gemm": (2 * bt * K * 2 * I * L,
-                                    n_touched * 2 * I * (L + 4) + bt * K * (L + 4) + bt * K * I),
-            "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * (I + 4) + bt * K * I + bt * K * L * b),
+            "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, n_touched * 2 * I * (L + 4)),
+            "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * (I + 4)),
             "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),
             "shared_gate_up_gemm": (2 * bt * S * 2 * Is * d, (S * 2 * Is * d + bt * d + bt * S * Is) * b),
             "up_shared_down_gemm": (2 * bt * d * (L + S * Is), (d * (L + S * Is) + bt * (L + S * Is) + bt * d) * b),
@@ -64,8 +66,8 @@ def algorithmic(shape, bt, n_touched, fp8_experts=False):
         "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
         "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
         "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
-        "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, (n_touched * 2 * I * L + bt * K * L + bt * K * I) * b),
-        "expert_down_gemm": (2 * bt * K * L * I, (n_touched * L * I + bt * K * I + bt * K * L) * b),
+        "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, n_touched * 2 * I * L * b),
+        "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * I * b),
         "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),
         "shared_gate_up_gemm": (2 * bt * S * 2 * Is * d, (S * 2 * Is * d + bt * d + bt * S * Is) * b),
         "up_shared_down_gemm": (2 * bt * d * (L + S * Is), (d * (L + S * Is) + bt * (L + S * Is) + bt * d) * b),
