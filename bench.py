@@ -53,6 +53,7 @@ def algorithmic(shape, bt, n_touched, fp8_experts=False):
             "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
             "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
             "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
+            "token_gather": (0, bt * L * b + 2 * bt * L + bt * K * L),
             "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, n_touched * 2 * I * (L + 4)),
             "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * (I + 4)),
             "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),
@@ -66,6 +67,7 @@ def algorithmic(shape, bt, n_touched, fp8_experts=False):
         "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
         "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
         "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
+        "token_gather": (0, (bt * L + bt * K * L) * b),
         "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, n_touched * 2 * I * L * b),
         "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * I * b),
         "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),

@@ -245,9 +245,10 @@ LMOE_API void lmoe_debug_fail_next_alloc(void);
  * recorded events and writes, per stage, the summed device milliseconds over the recorded
  * calls into ms[LMOE_NUM_STAGES], the number of recorded calls into *calls and the number
  * of kernels those calls launched into *launches (any output may be NULL). */
-#define LMOE_NUM_STAGES 8
-/* stage order: router GEMM, cutoff + top-K + segments, W_down GEMM, expert gate/up GEMM,
- * expert down GEMM, RMSNorm + combine, shared gate/up GEMM, W_up + shared-down GEMM */
+#define LMOE_NUM_STAGES 9
+/* stage order: router GEMM, cutoff + top-K + segments, W_down GEMM, routed token rows into slot
+ * order (gather; e4m3 quantization too with fp8 experts), expert gate/up GEMM, expert down GEMM,
+ * RMSNorm + combine, shared gate/up GEMM, W_up + shared-down GEMM */
 LMOE_API lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable);
 LMOE_API lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t* launches);
 

@@ -918,7 +918,25 @@ void tc_plan_destroy(TcPlan* plan) { delete plan; }
 
 void tc_inject_wait_timeout(TcPlan* plan) { plan->inject = true; }
 
-int tc_launches(int op, bool f8) { return op == kOpExpertGateUp ? (f8 ? 3 : 2) : 1; }
+int tc_launches(int op, bool f8) { (void)op; (void)f8; return 1; }
+
+cudaError_t tc_gather_tokens(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* n) {
+  const lmoe_config& c = pl->cfg;
+  const void* rows = pl->buf.z;
+  int vec = c.latent / 8;
+  *n = 1;
+  if (pl->f8) {
+    cudaError_t e = launch_quantize_rows(pl->buf.z, a.bt_tokens, c.latent, pl->buf.zq, pl->buf.tscale,
+                                         pl->sm_count * 8, st);
+    if (e != cudaSuccess) return e;
+    rows = pl->buf.zq;
+    vec = c.latent / 16;
+    *n = 2;
+  }
+  gather_rows_kernel<<<pl->sm_count * 8, 256, 0, st>>>(static_cast<const uint4*>(rows), a.a_rows, a.seg_off, a.G, vec,
+                                                       static_cast<uint4*>(pl->buf.zp));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   const lmoe_config& c = pl->cfg;
@@ -979,16 +997,8 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
         p.timeout_ns = kInjectTimeoutNs;
         pl->inject = false;
       }
-      // the experts' token rows (z, or its e4m3 copy quantized once per token), gathered once
-      // into slot order
-      const void* rows = pl->buf.z;
-      int vec = c.latent / 8;
+      // token rows: the slot-ordered copy tc_gather_tokens made (bf16, or e4m3 with per-token scales)
       if (pl->f8) {
-        cudaError_t e = launch_quantize_rows(pl->buf.z, a.bt_tokens, c.latent, pl->buf.zq, pl->buf.tscale,
-                                             pl->sm_count * 8, st);
-        if (e != cudaSuccess) return e;
-        rows = pl->buf.zq;
-        vec = c.latent / 16;
         maps.w[0] = pl->m_gate8;
         maps.wup = pl->m_up8;
         maps.tok = pl->m_zq8;
@@ -1004,10 +1014,6 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
         maps.wup = pl->m_up;
         maps.tok = pl->m_zp;
       }
-      gather_rows_kernel<<<pl->sm_count * 8, 256, 0, st>>>(static_cast<const uint4*>(rows), a.a_rows, a.seg_off, a.G,
-                                                           vec, static_cast<uint4*>(pl->buf.zp));
-      const cudaError_t ge = cudaGetLastError();
-      if (ge != cudaSuccess) return ge;
       p.w_group_rows = c.expert_inter;
       p.seg_off = a.seg_off;
       p.mtile_off = a.mtile_off;

@@ -32,6 +32,10 @@ void tc_plan_destroy(TcPlan* plan);
 void tc_inject_wait_timeout(TcPlan* plan);
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
 int tc_launches(int op, bool f8);   // kernels launch_gemm_tc starts for one GemmOp
+// The routed experts' token rows in slot order for the next expert gate/up GEMM (a = its
+// GemmArgs): z rows gathered through the slot -> token map, or, with e4m3 experts, z
+// quantized once per token and its e4m3 rows gathered.  Returns the kernels launched in *n.
+cudaError_t tc_gather_tokens(TcPlan* plan, const GemmArgs& a, cudaStream_t st, int* n);
 
 // Dense SiTU-GLU FFN (out = W_down act(W_gate x, W_up x)) on the same engine: descriptors of
 // the borrowed weights and of the caller-provided h [max_bt, inter] buffer.

@@ -91,7 +91,7 @@ void prof_mark(lmoe_ctx* ctx, int boundary, cudaStream_t st) {
 // NVTX ranges of a forward: "lmoe_forward" around the call, one range per stage inside it
 // (host-side annotations that profilers align with the kernels each stage launches).
 const char* const kStageNames[LMOE_NUM_STAGES] = {
-    "router GEMM", "cutoff + top-K + segments", "W_down GEMM", "expert gate/up GEMM",
+    "router GEMM", "cutoff + top-K + segments", "W_down GEMM", "token gather", "expert gate/up GEMM",
     "expert down GEMM", "RMSNorm + combine", "shared gate/up GEMM", "W_up + shared down GEMM"};
 
 void nvtx_stage(lmoe_ctx* ctx, int boundary) {
@@ -551,8 +551,14 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     g.bt_tokens = bt;
     g.epi = kEpiGlu; g.out = ctx->h; g.ldo = c.expert_inter;
     g.op = kOpExpertGateUp;
-    e = run_gemm(ctx, g, st);
+    if (ctx->use_tc) {  // the experts' token rows into slot order (the CUDA-core engine reads them through perm)
+      int n = 0;
+      e = tc_gather_tokens(ctx->tc, g, st, &n);
+      ctx->launches += n;
+    }
     stage_mark(ctx, 4, st);
+    if (e == cudaSuccess) e = run_gemm(ctx, g, st);
+    stage_mark(ctx, 5, st);
   }
   if (e == cudaSuccess) {  // y[slot] = W_d[e] h[slot]
     GemmArgs g = base_args(ctx);
@@ -564,7 +570,7 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     g.epi = kEpiStore; g.out = ctx->y; g.ldo = c.latent;
     g.op = kOpExpertDown;
     e = run_gemm(ctx, g, st);
-    stage_mark(ctx, 5, st);
+    stage_mark(ctx, 6, st);
   }
   if (e == cudaSuccess) {  // c = sum_k w RMSNorm(y_k) -> cat[:, 0:L]
     CombineArgs a;
@@ -574,7 +580,7 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     a.norm_sum = ctx->norm_sum;
     e = launch_combine(a, ctx->bf16, st);
     ctx->launches += 1;
-    stage_mark(ctx, 6, st);
+    stage_mark(ctx, 7, st);
   }
   if (e == cudaSuccess) {  // shared activations -> cat[:, L:]
     GemmArgs g = base_args(ctx);
@@ -586,7 +592,7 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     g.out = static_cast<char*>(ctx->cat) + (size_t)c.latent * ctx->esz; g.ldo = ldc;
     g.op = kOpSharedGateUp;
     e = run_gemm(ctx, g, st);
-    stage_mark(ctx, 7, st);
+    stage_mark(ctx, 8, st);
   }
   if (e == cudaSuccess) {  // out = [c | h_sh] [W_up | W_d^sh_0 | ...]^T
     GemmArgs g = base_args(ctx);
@@ -604,7 +610,7 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     g.epi = kEpiStore; g.out = out; g.ldo = c.d;
     g.op = kOpFinal;
     e = run_gemm(ctx, g, st);
-    stage_mark(ctx, 8, st);
+    stage_mark(ctx, 9, st);
   }
   if (ctx->prof_on && ctx->prof_calls < kProfCap) ctx->prof_calls++;
   nvtx_end(ctx);

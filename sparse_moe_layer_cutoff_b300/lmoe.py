@@ -180,8 +180,8 @@ def lmoe_workspace(ctx) -> lmoe_workspace_view:
     return v
 
 
-LMOE_NUM_STAGES = 8
-STAGE_NAMES = ("router_gemm", "cutoff_topk_segments", "w_down_gemm", "expert_gate_up_gemm",
+LMOE_NUM_STAGES = 9
+STAGE_NAMES = ("router_gemm", "cutoff_topk_segments", "w_down_gemm", "token_gather", "expert_gate_up_gemm",
                "expert_down_gemm", "rmsnorm_combine", "shared_gate_up_gemm", "up_shared_down_gemm")
 
 
