@@ -18,7 +18,7 @@
 // Accumulators: TMEM holds 512 fp32 columns in two 256-column slots.  A tile of at most
 // 128 tokens takes one slot (A0 in its first 128 columns, A1 in the second), so two such
 // tiles double-buffer; a wider tile takes both slots (A0 in slot 0, A1 in slot 1).
-// Roles (512 threads): warp 0 streams weight tiles through a kWStages ring, warp 2 streams
+// Roles (512 threads): warp 0 streams weight tiles through a 4-stage ring, warp 2 streams
 // token tiles through a kTStages ring (TMA, mbarrier completion), warp 1 owns TMEM and
 // issues tcgen05.mma (one thread), warps 4-15 drain the accumulators with tcgen05.ld (three
 // warps per TMEM lane quadrant, taking every third 32-token chunk) and write the outputs.
@@ -46,7 +46,6 @@ constexpr int kTokMax = kTileM;                  // tokens per tile of the group
 constexpr int kTokBox = 16;                      // token rows per TMA box
 constexpr int kHalfBytes = kHalf * kBK * 2;      // 16 KB
 constexpr int kWStageBytes = 2 * kHalfBytes;     // 32 KB of weights per stage
-constexpr int kWStages = 4;
 constexpr int kTStages = 3;
 constexpr int kSlotCols = 256;
 constexpr int kEpiWarps = 12;
@@ -55,8 +54,6 @@ constexpr int kThreads = 128 + kEpiThreads;
 constexpr int kStaged = 2;                       // 32-token chunks an epilogue warp keeps in registers
 constexpr int kSchedMax = 1024;                  // schedule entries kept in shared memory
 constexpr int kDenseGroup = 8;                   // token tiles per raster group (dense GEMMs)
-// barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
-constexpr int kNumBars = 2 * kWStages + 2 * kTStages + 4 + 1;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
 
@@ -67,6 +64,9 @@ constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a tim
 template <bool DENSE>
 struct Geo {
   static constexpr int kTok = DENSE ? 256 : kTokMax;             // tokens per tile at most
+  static constexpr int kWStages = 4;                             // weight ring (32 KB stages)
+  // barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
+  static constexpr int kNumBars = 2 * kWStages + 2 * kTStages + 4 + 1;
   static constexpr int kTStageBytes = kTok * kBK * 2;            // token rows per stage
   static constexpr int kChunks = (kTok / 32 + 2) / 3;           // 32-token chunks per epilogue warp
   static constexpr int kOffT = kWStages * kWStageBytes;
@@ -370,16 +370,16 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t bar0 = smem_u32(bars);
   auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
-  auto wempty_bar = [&](int s) { return bar0 + 8u * (kWStages + s); };
-  auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * kWStages + s); };
-  auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * kWStages + kTStages + s); };
-  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * kWStages + 2 * kTStages + a); };
-  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * kWStages + 2 * kTStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kWStages + 2 * kTStages + 4);
+  auto wempty_bar = [&](int s) { return bar0 + 8u * (G::kWStages + s); };
+  auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * G::kWStages + s); };
+  auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * G::kWStages + kTStages + s); };
+  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * G::kWStages + 2 * kTStages + a); };
+  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * G::kWStages + 2 * kTStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * G::kWStages + 2 * kTStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kWStages; ++s) { mbar_init(wfull_bar(s), 1); mbar_init(wempty_bar(s), 1); }
+    for (int s = 0; s < G::kWStages; ++s) { mbar_init(wfull_bar(s), 1); mbar_init(wempty_bar(s), 1); }
     for (int s = 0; s < kTStages; ++s) { mbar_init(tfull_bar(s), 1); mbar_init(tempty_bar(s), 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(afull_bar(a), 1); mbar_init(aempty_bar(a), kEpiWarps); }
     mbar_init(drain_bar, 1);
@@ -446,12 +446,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           }
           pending |= 1u << stage;
           pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == kWStages) { stage = 0; phase ^= 1u; }
+          if (++stage == G::kWStages) { stage = 0; phase ^= 1u; }
         }
       }
       if (stop) {
         // no copy may still be landing in shared memory when the block exits
-        for (int s = 0; s < kWStages; ++s)
+        for (int s = 0; s < G::kWStages; ++s)
           if (pending & (1u << s)) mbar_wait(wfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, p.timeout_ns, false);
       }
     }
@@ -533,7 +533,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           issued = true;
           tc_commit(wempty_bar(ws));
           tc_commit(tempty_bar(ts));
-          if (++ws == kWStages) { ws = 0; wph ^= 1u; }
+          if (++ws == G::kWStages) { ws = 0; wph ^= 1u; }
           if (++ts == kTStages) { ts = 0; tph ^= 1u; }
         }
         if (stop) break;
