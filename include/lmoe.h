@@ -106,7 +106,7 @@ typedef struct lmoe_ctx lmoe_ctx;
 typedef void* lmoe_stream; /* a cudaStream_t */
 
 /* Validate cfg and weights, build the tensor-memory descriptors for the borrowed weights and
- * allocate the workspace for up to max_bt tokens (about bt*K*(I + latent)*2 bytes plus
+ * allocate the workspace for up to max_bt tokens (about bt*K*(I + 2*latent)*2 bytes plus
  * O(bt*(E + d)) for bf16) on the current device.  Launches nothing; `stream` is only
  * recorded as the context's default.  On success *out owns the context (free with
  * lmoe_destroy); on any error *out is set to NULL and nothing stays allocated. */

@@ -267,6 +267,29 @@ def test_near_tie_routing_is_exact(scale_log2):
     r.check_output(ref_route=ref)
 
 
+def test_tied_expert_group_routes_exactly():
+    """Forty experts with the same router row (bit-identical logits, so the same score and, over
+    the batch, the same cutoff: 40-way ties in every token).  Tokens whose top-K reaches into the
+    tied group cannot be decided from at most 32 candidates, so the top-K of those tokens runs in
+    the general kernel while the others stay on the register fast path; the selection (ties to the
+    lower expert index) must match the oracle bit for bit either way."""
+    w = WORKLOADS["small_bf16"].with_(seed=23)
+    x, weights, bias = make_inputs(w, "cuda", 512)
+    wr = weights["w_router"].clone()
+    wr[:40] = wr[0]
+    weights = dict(weights, w_router=wr.contiguous())
+    r = Run(w, x=x, weights=weights, bias=bias)
+    assert r.status == 0
+    logits = r.route["logits"]
+    assert torch.equal(logits[:, :40], logits[:, :1].expand(-1, 40))     # the group is tied exactly
+    ref = r.check_routing()
+    idx = ref["idx"]
+    in_group = (idx < 40).sum(axis=1)
+    # both kinds of token occur: some select from the tied group (general kernel), some do not
+    assert 0 < int((in_group > 0).sum()) < idx.shape[0]
+    r.check_output(ref_route=ref)
+
+
 def test_streaming_cutoff_matches_oracle():
     """lmoe_set_cutoff_momentum: each call's cutoff is m * previous + (1 - m) * the call's
     quantile, carried in the context; routing stays bit-exact against the oracle's
