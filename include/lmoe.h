@@ -107,7 +107,8 @@ typedef void* lmoe_stream; /* a cudaStream_t */
 
 /* Validate cfg and weights, build the tensor-memory descriptors for the borrowed weights and
  * allocate the workspace for up to max_bt tokens (about bt*K*(I + 2*latent)*2 bytes plus
- * O(bt*(E + d)) for bf16) on the current device.  Launches nothing; `stream` is only
+ * O(bt*(E + d)) for bf16, and 256 KB per SM of fp32 partial sums for the dense GEMMs that
+ * small batches split along K) on the current device.  Launches nothing; `stream` is only
  * recorded as the context's default.  On success *out owns the context (free with
  * lmoe_destroy); on any error *out is set to NULL and nothing stays allocated. */
 LMOE_API lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt,

@@ -54,6 +54,10 @@ constexpr int kThreads = 128 + kEpiThreads;
 constexpr int kStaged = 2;                       // 32-token chunks an epilogue warp keeps in registers
 constexpr int kSchedMax = 1024;                  // schedule entries kept in shared memory
 constexpr int kDenseGroup = 8;                   // token tiles per raster group (dense GEMMs)
+constexpr int kPartRows = 2 * kHalf;            // split-K partials: weight rows per tile
+constexpr int kPartItem = kPartRows * 256;       // fp32 values per work item ([token][row], <= 256 tokens)
+constexpr int kSplitMinKb = 4;                   // k-blocks per split at least
+static_assert(kPartItem == kTcPartPerSm, "one work item of partials per SM at most");
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
 
@@ -95,6 +99,8 @@ struct TcParams {
   int kblocks;              // K / 64
   int bt;                   // dense: tokens
   int tok_tile;             // dense: tokens per tile (<= kTokMax, multiple of 16)
+  int ksplit;               // dense: work items per tile, each over its own K range (1 = whole K)
+  float* part;              // split-K: fp32 accumulators, kPartItem per work item
   const int32_t* seg_off;   // grouped: [G + 1] token segments
   const int32_t* mtile_off; // grouped: [G + 1] prefix of kTokMax-token tiles
   int G;                    // grouped: number of groups, 0 for dense
@@ -337,6 +343,23 @@ __device__ __forceinline__ int k_rot(const TcParams& p, const Tile& tl, int kb) 
   return k >= p.kblocks ? k - p.kblocks : k;
 }
 
+// Work item t of a launch: its tile and k-block range [kb0, kb1).  Split-K launches (dense
+// GEMMs with too few tiles to fill the GPU) give each tile ksplit consecutive items, item ks
+// covering k-blocks [ks * kblocks / ksplit, (ks + 1) * kblocks / ksplit) in order.
+template <bool SPLIT>
+__device__ __forceinline__ Tile decode_work(const TcParams& p, const int32_t* seg, const int32_t* mt, int t, int& kb0,
+                                            int& kb1) {
+  if (!SPLIT) {
+    kb0 = 0;
+    kb1 = p.kblocks;
+    return decode_tile(p, seg, mt, t);
+  }
+  const int tile = t / p.ksplit, ks = t - tile * p.ksplit;
+  kb0 = (int)((long long)ks * p.kblocks / p.ksplit);
+  kb1 = (int)((long long)(ks + 1) * p.kblocks / p.ksplit);
+  return decode_tile(p, seg, mt, tile);
+}
+
 // Weight operands of a tile: GLU always two (gate, up); store / router one or two blocks
 // of 128 output rows.
 template <int EPI>
@@ -352,9 +375,10 @@ __device__ __forceinline__ uint32_t acc_col(bool wide, int slot, int h) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int EPI, bool F8, bool DENSE>
+template <int EPI, bool F8, bool DENSE, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  static_assert(!SPLIT || (DENSE && !F8), "split-K covers the dense bf16 GEMMs");
   using G = Geo<DENSE>;
   constexpr int kBKe = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
   extern __shared__ uint8_t smem_raw[];
@@ -404,7 +428,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   const uint32_t tmem_base = *tmem_slot;
   const int32_t* seg = sched_smem ? s_seg : p.seg_off;
   const int32_t* mt = sched_smem ? s_mt : p.mtile_off;
-  const int ntiles = num_tiles(p);
+  const int nwork = SPLIT ? num_tiles(p) * p.ksplit : num_tiles(p);
 
   if (warp == 0) {
     // ---------------------------------------------------------------- weight producer
@@ -430,10 +454,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       int stage = 0;
       uint32_t phase = 0, pending = 0, pend_parity = 0;
       bool stop = false;
-      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
-        const Tile tl = decode_tile(p, seg, mt, t);
+      for (int t = blockIdx.x; t < nwork && !stop; t += gridDim.x) {
+        int kb0, kb1;
+        const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
         const int nh = tile_halves<EPI>(p, tl);
-        for (int kb = 0; kb < p.kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(wempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           pending &= ~(1u << stage);
           mbar_expect_tx(wfull_bar(stage), (uint32_t)(nh * kHalfBytes));
@@ -441,7 +466,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           for (int h = 0; h < nh; ++h) {
             const CUtensorMap* m;
             int x, y;
-            w_src(tl, k_rot(p, tl, kb), h, m, x, y);
+            w_src(tl, SPLIT ? kb : k_rot(p, tl, kb), h, m, x, y);
             tma_load_2d(dst + h * kHalfBytes, m, x, y, wfull_bar(stage), wpol);
           }
           pending |= 1u << stage;
@@ -462,11 +487,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     int stage = 0;
     uint32_t phase = 0, pending = 0, pend_parity = 0;
     bool stop = false;
-    for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
-      const Tile tl = decode_tile(p, seg, mt, t);
+    for (int t = blockIdx.x; t < nwork && !stop; t += gridDim.x) {
+      int kb0, kb1;
+      const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
       const int ntr = (tl.ntok + 15) & ~15;
       const int nbox = ntr / kTokBox;
-      for (int kb = 0; kb < p.kblocks; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait(tempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns);
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -481,7 +507,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         __syncwarp();
         const uint32_t dst = tbase + stage * G::kTStageBytes;
         if (lane < nbox)
-          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, k_rot(p, tl, kb) * kBKe, tl.tok0 + lane * kTokBox,
+          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, (SPLIT ? kb : k_rot(p, tl, kb)) * kBKe,
+                      tl.tok0 + lane * kTokBox,
                       tfull_bar(stage), tpol);
         pending |= 1u << stage;
         pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
@@ -500,8 +527,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       uint32_t wph = 0, tph = 0;
       uint32_t aph[2] = {0u, 0u};
       bool stop = false, issued = false;
-      for (int t = blockIdx.x; t < ntiles && !stop; t += gridDim.x) {
-        const Tile tl = decode_tile(p, seg, mt, t);
+      for (int t = blockIdx.x; t < nwork && !stop; t += gridDim.x) {
+        int kb0, kb1;
+        const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
         const int ntr = (tl.ntok + 15) & ~15;
         const bool wide = ntr > kHalf;
         const int nh = tile_halves<EPI>(p, tl);
@@ -515,7 +543,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc_col(wide, slot, 0);
         const uint32_t d1 = tmem_base + acc_col(wide, slot, 1);
-        for (int kb = 0; kb < p.kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(wfull_bar(ws), wph, abort_flag, p.status, p.timeout_ns) ||
               !mbar_wait(tfull_bar(ts), tph, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           tc_fence_after();
@@ -523,12 +551,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           const uint64_t bd = smem_desc(tbase + ts * G::kTStageBytes);
 #pragma unroll
           for (int j = 0; j < kBK / 16; ++j)
-            tc_mma_k<F8>(d0, ad + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+            tc_mma_k<F8>(d0, ad + 2u * j, bd + 2u * j, idesc, (kb != kb0 || j != 0) ? 1u : 0u);
           if (nh == 2) {
             const uint64_t ad1 = ad + (uint64_t)(kHalfBytes >> 4);
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j)
-              tc_mma_k<F8>(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb | j) != 0 ? 1u : 0u);
+              tc_mma_k<F8>(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb != kb0 || j != 0) ? 1u : 0u);
           }
           issued = true;
           tc_commit(wempty_bar(ws));
@@ -561,8 +589,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
     const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
     int slot = 0;
     uint32_t aph[2] = {0u, 0u};
-    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-      const Tile tl = decode_tile(p, seg, mt, t);
+    for (int t = blockIdx.x; t < nwork; t += gridDim.x) {
+      int kb0, kb1;
+      const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
       const int ntr = (tl.ntok + 15) & ~15;
       const bool wide = ntr > kHalf;
       const int nh = tile_halves<EPI>(p, tl);
@@ -597,7 +626,23 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       // Results of this warp's first kStaged chunks stay in registers and are written after
       // TMEM is released; later chunks (tiles of more than 192 tokens) are written at once.
       uint32_t res[kStaged][2][16];
-      if (EPI == kEpiGlu) {
+      if (SPLIT) {
+        // the raw fp32 accumulators of this work item, part[t][token][row] (row = 128 h + TMEM
+        // lane): for each token the 32 lanes of a warp write 128 consecutive bytes
+        float* wp = p.part + (long long)t * kPartItem;
+        for (int c = sub; c < nchunks; c += 3) {
+          const int nj = min(32, tl.ntok - c * 32);
+          for (int h = 0; h < nh; ++h) {
+            uint32_t v[32];
+            tmem_ld32((h ? c1 : c0) + c * 32, v);
+            tmem_wait_ld();
+            float* o = wp + (long long)(c * 32) * kPartRows + h * kHalf + q * 32 + lane;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nj) o[j * kPartRows] = __uint_as_float(v[j]);
+          }
+        }
+      } else if (EPI == kEpiGlu) {
         // fp8: per-row weight scales of this lane's feature (gate and up rows)
         float sg = 1.f, su = 1.f;
         if (F8) {
@@ -712,7 +757,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         if (wide) { mbar_arrive(aempty_bar(0)); mbar_arrive(aempty_bar(1)); }
         else mbar_arrive(aempty_bar(slot));
       }
-      if (EPI != kEpiRouter) {
+      if (EPI != kEpiRouter && !SPLIT) {
 #pragma unroll
         for (int ci = 0; ci < kStaged; ++ci) {
           const int c = sub + 3 * ci;
@@ -731,6 +776,42 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   __syncthreads();
   tc_fence_after();
   if (warp == 1) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kSlotCols));
+}
+
+// Split-K reduction and epilogue: sums the ksplit partial accumulators of every (tile, token,
+// weight row) in the fixed order ks = 0, 1, ... (so results are deterministic) and applies the
+// launch's epilogue: bf16 store, SiTU-GLU of the gate and up sums, or the router's fp32 logits
+// plus bias and their transposed copy.  tt = tokens per tile index range (<= tok_tile).
+template <int EPI>
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcParams p, int tt) {
+  constexpr int R = EPI == kEpiGlu ? kHalf : 2 * kHalf;   // output rows of a tile
+  const long long total = (long long)num_tiles(p) * tt * R;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i % R);
+    const long long q = i / R;
+    const int tok = (int)(q % tt);
+    const int T = (int)(q / tt);
+    const Tile tl = decode_tile(p, nullptr, nullptr, T);
+    if (tok >= tl.ntok) continue;
+    const int f = EPI == kEpiGlu ? tl.fb * kHalf + r : tl.fb * 2 * kHalf + r;
+    if (f >= p.n_feat) continue;
+    const float* src = p.part + (long long)T * p.ksplit * kPartItem + (long long)tok * kPartRows + r;
+    float s0 = 0.f, s1 = 0.f;
+    for (int ks = 0; ks < p.ksplit; ++ks) {
+      s0 += src[(long long)ks * kPartItem];
+      if (EPI == kEpiGlu) s1 += src[(long long)ks * kPartItem + kHalf];
+    }
+    const long long row = tl.tok0 + tok;
+    if (EPI == kEpiGlu) {
+      static_cast<bf16*>(p.out)[row * p.ldo + f] = __float2bfloat16_rn(situ_glu_fast(s0, s1, p));
+    } else if (EPI == kEpiStore) {
+      static_cast<bf16*>(p.out)[row * p.ldo + f] = __float2bfloat16_rn(s0);
+    } else {
+      const float v = s0 + (p.bias ? p.bias[f] : 0.f);
+      static_cast<float*>(p.out)[row * p.ldo + f] = v;
+      p.out_t[(long long)f * p.ldt + row] = v;
+    }
+  }
 }
 
 // Routed-expert token rows in slot order: zp[slot] = rows[perm[slot]] (z, or its e4m3 copy);
@@ -801,21 +882,45 @@ int dense_tok_tile(int bt, int n_fb, int grid) {
   return best;
 }
 
-template <int EPI, bool F8, bool DENSE>
+template <int EPI, bool F8, bool DENSE, bool SPLIT = false>
 cudaError_t launch_kernel(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t st) {
-  tc_gemm_kernel<EPI, F8, DENSE><<<grid, kThreads, Geo<DENSE>::kSmemBytes, st>>>(maps, p);
+  tc_gemm_kernel<EPI, F8, DENSE, SPLIT><<<grid, kThreads, Geo<DENSE>::kSmemBytes, st>>>(maps, p);
   return cudaGetLastError();
 }
 
-// One launch of the persistent kernel: grid = SMs (fewer when a dense GEMM has fewer tiles).
-cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st, bool f8 = false) {
+// A dense split-K GEMM: the partial products, then their reduction with the epilogue.
+template <int EPI>
+cudaError_t launch_split(const TcMaps& maps, const TcParams& p, int grid, int sm_count, cudaStream_t st) {
+  cudaError_t e = launch_kernel<EPI, false, true, true>(maps, p, grid, st);
+  if (e != cudaSuccess) return e;
+  const int tt = p.tok_tile < p.bt ? p.tok_tile : p.bt;
+  const long long total = (long long)((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb * tt * (EPI == kEpiGlu ? kHalf : 2 * kHalf);
+  long long blocks = (total + 255) / 256;
+  if (blocks > (long long)sm_count * 8) blocks = (long long)sm_count * 8;
+  splitk_reduce_kernel<EPI><<<(int)blocks, 256, 0, st>>>(p, tt);
+  return cudaGetLastError();
+}
+
+// One GEMM: the persistent kernel with grid = SMs (fewer when a dense GEMM has fewer work
+// items).  A dense GEMM with at most half as many tiles as SMs and a partial buffer
+// (p.part) is split along K into up to SMs / tiles work items per tile (each of at least
+// kSplitMinKb k-blocks) and reduced by a second kernel.  *n = kernels launched.
+cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st, bool f8, int* n) {
+  *n = 0;
+  p.ksplit = 1;
   if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, sm_count);
   int grid = sm_count;
   if (p.G == 0) {
     const long long tiles = (long long)((p.bt + p.tok_tile - 1) / p.tok_tile) * p.n_fb;
-    if (tiles < grid) grid = (int)tiles;
+    if (p.part && tiles > 0 && 2 * tiles <= sm_count) {
+      long long s = sm_count / tiles;
+      if (s > p.kblocks / kSplitMinKb) s = p.kblocks / kSplitMinKb;
+      if (s >= 2) p.ksplit = (int)s;
+    }
+    if (tiles * p.ksplit < grid) grid = (int)(tiles * p.ksplit);
   }
   if (grid <= 0) return cudaSuccess;
+  *n = p.ksplit > 1 ? 2 : 1;
   if (f8) {   // the fp8 routed experts (grouped)
     if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false>(maps, p, grid, st);
     return launch_kernel<kEpiStore, true, false>(maps, p, grid, st);
@@ -824,6 +929,13 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
     if (epi == kEpiGlu) return launch_kernel<kEpiGlu, false, false>(maps, p, grid, st);
     return launch_kernel<kEpiStore, false, false>(maps, p, grid, st);
   }
+  if (p.ksplit > 1) {
+    switch (epi) {
+      case kEpiStore: return launch_split<kEpiStore>(maps, p, grid, sm_count, st);
+      case kEpiGlu: return launch_split<kEpiGlu>(maps, p, grid, sm_count, st);
+      default: return launch_split<kEpiRouter>(maps, p, grid, sm_count, st);
+    }
+  }
   switch (epi) {
     case kEpiStore: return launch_kernel<kEpiStore, false, true>(maps, p, grid, st);
     case kEpiGlu: return launch_kernel<kEpiGlu, false, true>(maps, p, grid, st);
@@ -831,9 +943,9 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
   }
 }
 
-template <int EPI, bool F8, bool DENSE>
+template <int EPI, bool F8, bool DENSE, bool SPLIT = false>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Geo<DENSE>::kSmemBytes);
 }
 
@@ -842,6 +954,9 @@ cudaError_t prepare_kernels(bool f8) {
   cudaError_t e = set_smem<kEpiStore, false, true>();
   if (e == cudaSuccess) e = set_smem<kEpiGlu, false, true>();
   if (e == cudaSuccess) e = set_smem<kEpiRouter, false, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiStore, false, true, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiGlu, false, true, true>();
+  if (e == cudaSuccess) e = set_smem<kEpiRouter, false, true, true>();
   if (e == cudaSuccess) e = set_smem<kEpiStore, false, false>();
   if (e == cudaSuccess) e = set_smem<kEpiGlu, false, false>();
   if (e == cudaSuccess && f8) e = set_smem<kEpiGlu, true, false>();
@@ -918,8 +1033,6 @@ void tc_plan_destroy(TcPlan* plan) { delete plan; }
 
 void tc_inject_wait_timeout(TcPlan* plan) { plan->inject = true; }
 
-int tc_launches(int op, bool f8) { (void)op; (void)f8; return 1; }
-
 cudaError_t tc_gather_tokens(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* n) {
   const lmoe_config& c = pl->cfg;
   const void* rows = pl->buf.z;
@@ -938,7 +1051,8 @@ cudaError_t tc_gather_tokens(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* n) {
+  *n = 0;
   const lmoe_config& c = pl->cfg;
   TcMaps maps;
   memset(&maps, 0, sizeof(maps));
@@ -957,6 +1071,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   p.inv_beta_u = 1.0f / a.beta_u;
   p.status = pl->buf.status;
   p.timeout_ns = kTimeoutNs;
+  p.part = pl->buf.part;   // dense GEMMs may split K (launch_tc decides)
   int epi = a.epi;
   bool ok = true, f8 = false;
   switch (a.op) {
@@ -1042,7 +1157,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st) {
   }
   if (!ok) return cudaErrorInvalidValue;
   p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
-  return launch_tc(maps, p, epi, pl->sm_count, st, f8);
+  return launch_tc(maps, p, epi, pl->sm_count, st, f8, n);
 }
 
 // ------------------------------------------------------------------ dense SiTU-GLU FFN
@@ -1116,7 +1231,8 @@ cudaError_t tc_ffn_forward(TcFfnPlan* pl, const void* x, int bt, void* out, cuda
       p.out = out;
       p.ldo = pl->d;
     }
-    const cudaError_t e = launch_tc(maps, p, pass == 0 ? kEpiGlu : kEpiStore, pl->sm_count, st);
+    int n;
+    const cudaError_t e = launch_tc(maps, p, pass == 0 ? kEpiGlu : kEpiStore, pl->sm_count, st, false, &n);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -16,6 +16,7 @@ struct TcBuffers {
   void* y;
   void* cat;
   float* tscale;     // [max_bt] per-token scales of zq (fp8 experts)
+  float* part;       // [sm_count * 65536] fp32 split-K partial accumulators of the dense GEMMs
   uint32_t* status;
 };
 
@@ -30,8 +31,10 @@ void tc_plan_destroy(TcPlan* plan);
 // shortens its waits to 20 ms, so the kernel times out, records LMOE timeout status and
 // returns.
 void tc_inject_wait_timeout(TcPlan* plan);
-cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st);
-int tc_launches(int op, bool f8);   // kernels launch_gemm_tc starts for one GemmOp
+// One GemmOp; *n = kernels launched (a dense GEMM split along K adds its reduction).
+cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st, int* n);
+// fp32 values of TcBuffers::part per SM
+constexpr long long kTcPartPerSm = 65536;
 // The routed experts' token rows in slot order for the next expert gate/up GEMM (a = its
 // GemmArgs): z rows gathered through the slot -> token map, or, with e4m3 experts, z
 // quantized once per token and its e4m3 rows gathered.  Returns the kernels launched in *n.

@@ -57,6 +57,7 @@ struct lmoe_ctx {
   void* y;
   void* cat;
   float* tscale;
+  float* part;          // split-K partials of the dense GEMMs (bf16 engine)
   uint32_t* status;
   TcPlan* tc;
   // per-stage profiling
@@ -232,8 +233,13 @@ lmoe_status finish(lmoe_ctx* ctx, cudaStream_t st, cudaError_t e) {
 }
 
 cudaError_t run_gemm(lmoe_ctx* ctx, const GemmArgs& g, cudaStream_t st) {
-  ctx->launches += ctx->use_tc ? tc_launches(g.op, ctx->f8) : 1;
-  if (ctx->use_tc) return launch_gemm_tc(ctx->tc, g, st);
+  if (ctx->use_tc) {
+    int n = 0;
+    const cudaError_t e = launch_gemm_tc(ctx->tc, g, st, &n);
+    ctx->launches += n;
+    return e;
+  }
+  ctx->launches += 1;
   return launch_gemm_simt(g, ctx->bf16, st);
 }
 
@@ -400,6 +406,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   size_t o_y = cv.take<char>(bt * K * L * ctx->esz);
   size_t o_cat = cv.take<char>(bt * ldc * ctx->esz);
   size_t o_tscale = cv.take<float>(bt);
+  size_t o_part = ctx->bf16 ? cv.take<float>((size_t)ctx->sm_count * kTcPartPerSm) : 0;
   ctx->ws_bytes = cv.off;
   if (ws_malloc(reinterpret_cast<void**>(&ctx->ws), ctx->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -428,6 +435,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->y = b + o_y;
   ctx->cat = b + o_cat;
   ctx->tscale = (float*)(b + o_tscale);
+  ctx->part = ctx->bf16 ? (float*)(b + o_part) : nullptr;
   if (cudaMemset(ctx->ws, 0, ctx->ws_bytes) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(ctx->ws);
@@ -447,6 +455,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
       TcBuffers tb;
       tb.z = ctx->z; tb.zq = ctx->zq; tb.zp = ctx->zp; tb.h = ctx->h; tb.y = ctx->y; tb.cat = ctx->cat;
       tb.tscale = ctx->tscale;
+      tb.part = ctx->part;
       tb.status = ctx->status;
       lmoe_status ts = tc_plan_create(&c, w, f8, max_bt, ctx->sm_count, tb, &ctx->tc);
       if (ts != LMOE_OK) {

@@ -9,7 +9,7 @@ from oracle import lmoe_oracle as O
 from sparse_moe_layer_cutoff_b300 import LatentMoE, LmoeError
 from sparse_moe_layer_cutoff_b300 import lmoe as L
 from sparse_moe_layer_cutoff_b300.lmoe import workspace_tensors
-from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, latent_norm_scale, oracle_weights, rel_l2, to64
+from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, GAP_MIN, latent_norm_scale, oracle_weights, rel_l2, to64
 from workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -80,7 +80,7 @@ def _run_fp8(wl, bt, rows=None, norm="expert"):
     torch.cuda.synchronize()
     assert layer.sync_status() == 0
     ref = O.route(to64(r["logits"]), s.top_k)
-    assert ref["min_gap"] > 1e-12
+    assert ref["min_gap"] > GAP_MIN
     np.testing.assert_array_equal(r["idx"].cpu().numpy(), ref["idx"])
     rows = np.arange(bt) if rows is None else np.asarray(rows)
     # the layer's stored z (bf16) enters the oracle's per-token quantizer, as the logits
