@@ -816,7 +816,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const TcParams p, in
 
 // Routed-expert token rows in slot order: zp[slot] = rows[perm[slot]] (z, or its e4m3 copy);
 // one warp per row, 16-byte vectors (HBM-bound: each row is read from L2-resident rows and
-// written once).
+// written once).  A lane issues its loads kGatherBatch at a time before storing them, so
+// enough bytes are in flight to cover the L2 latency.
+constexpr int kGatherBatch = 7;   // 3584-wide rows: 14 (bf16) or 7 (e4m3) vectors per lane
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ rows, const int32_t* __restrict__ perm,
                                                           const int32_t* __restrict__ offsets, int n_experts,
                                                           int vec_per_row, uint4* __restrict__ zp) {
@@ -826,7 +828,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
   for (int slot = blockIdx.x * wpb + (threadIdx.x >> 5); slot < nslots; slot += gridDim.x * wpb) {
     const uint4* src = rows + (long long)perm[slot] * vec_per_row;
     uint4* dst = zp + (long long)slot * vec_per_row;
-    for (int v = lane; v < vec_per_row; v += 32) dst[v] = src[v];
+    int v = lane;
+    for (; v + 32 * (kGatherBatch - 1) < vec_per_row; v += 32 * kGatherBatch) {
+      uint4 r[kGatherBatch];
+#pragma unroll
+      for (int i = 0; i < kGatherBatch; ++i) r[i] = src[v + 32 * i];
+#pragma unroll
+      for (int i = 0; i < kGatherBatch; ++i) dst[v + 32 * i] = r[i];
+    }
+    for (; v < vec_per_row; v += 32) dst[v] = src[v];
   }
 }
 

@@ -392,15 +392,18 @@ topk_fast_kernel(const float* __restrict__ logits, const double* __restrict__ al
       nc += __popc(m);
     }
     __syncwarp();
-    // exact ranks: fp32 order for candidates further apart than 2 tol, fp64 keys otherwise
+    // exact ranks: fp32 order for candidates further apart than 2 tol, fp64 keys otherwise.
+    // Each candidate's fp64 score is computed once (one pass of the narrow fp64 pipe per
+    // token) and serves both its fp64 key and, if chosen, its combine weight.
     const int ej = lane < nc ? cid[lane] : 0;
     const float kj32 = lane < nc ? ck32[lane] : 0.f;
+    const double sj = lane < nc ? sigmoid_f64((double)lrow[ej]) : 0.0;
     bool near = false;
     if (lane < nc)
       for (int i = 0; i < nc; ++i)
         if (i != lane && fabsf(ck32[i] - kj32) <= 2.0f * kKeyTol) near = true;
     if (__any_sync(full, near)) {
-      if (near) ck64[lane] = sigmoid_f64((double)lrow[ej]) - s_alpha[ej];
+      if (near) ck64[lane] = sj - s_alpha[ej];
       __syncwarp();
     }
     if (lane < nc) {
@@ -418,7 +421,7 @@ topk_fast_kernel(const float* __restrict__ logits, const double* __restrict__ al
       }
       if (rank < top_k) {
         idx_out[(size_t)t * top_k + rank] = ej;
-        chosen_s[rank] = sigmoid_f64((double)lrow[ej]);
+        chosen_s[rank] = sj;
       }
     }
     __syncwarp();
