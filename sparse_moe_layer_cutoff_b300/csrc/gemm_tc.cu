@@ -155,10 +155,11 @@ __device__ __forceinline__ unsigned long long global_ns() {
 }
 
 // Bounded wait.  Gives up when the deadline passes (setting abort + timeout status) or,
-// if honour_abort, as soon as another role has aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       uint32_t* status, unsigned long long limit_ns, bool honour_abort = true) {
-  if (mbar_test(bar, parity)) return true;
+// if honour_abort, as soon as another role has aborted.  The phase test is inlined and only a
+// wait that does not pass at once calls the polling loop: the MMA issuer's loop runs one such
+// test per ring stage, and a call there (stack frame and all) slowed the expert GEMMs by 6 %.
+__device__ __noinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            uint32_t* status, unsigned long long limit_ns, bool honour_abort) {
   const unsigned long long t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_test(bar, parity)) return true;
@@ -171,6 +172,10 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
       }
     }
   }
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, uint32_t* status,
+                                          unsigned long long limit_ns, bool honour_abort = true) {
+  return mbar_test(bar, parity) || mbar_wait_poll(bar, parity, abort_flag, status, limit_ns, honour_abort);
 }
 
 // 2-D TMA tile load into shared memory, completing on an mbarrier, with an L2 policy.
@@ -338,8 +343,12 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int32_t* se
 // same time and read the same token rows, so each starts its K loop at a different
 // offset (evenly spread); every token k-block is then fetched from DRAM by one CTA and
 // found in L2 by the others.  The order is fixed per tile, so results are deterministic.
-__device__ __forceinline__ int k_rot(const TcParams& p, const Tile& tl, int kb) {
-  int k = kb + (int)(((long long)tl.fb * p.kblocks) / p.n_fb);
+// k_start is computed once per tile; k_at maps the tile's kb-th k-block.
+__device__ __forceinline__ int k_start(const TcParams& p, const Tile& tl) {
+  return (int)(((long long)tl.fb * p.kblocks) / p.n_fb);
+}
+__device__ __forceinline__ int k_at(const TcParams& p, int rot, int kb) {
+  const int k = kb + rot;
   return k >= p.kblocks ? k - p.kblocks : k;
 }
 
@@ -458,6 +467,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         int kb0, kb1;
         const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
         const int nh = tile_halves<EPI>(p, tl);
+        const int rot = SPLIT ? 0 : k_start(p, tl);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(wempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           pending &= ~(1u << stage);
@@ -466,7 +476,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           for (int h = 0; h < nh; ++h) {
             const CUtensorMap* m;
             int x, y;
-            w_src(tl, SPLIT ? kb : k_rot(p, tl, kb), h, m, x, y);
+            w_src(tl, k_at(p, rot, kb), h, m, x, y);
             tma_load_2d(dst + h * kHalfBytes, m, x, y, wfull_bar(stage), wpol);
           }
           pending |= 1u << stage;
@@ -492,6 +502,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
       const int ntr = (tl.ntok + 15) & ~15;
       const int nbox = ntr / kTokBox;
+      const int rot = SPLIT ? 0 : k_start(p, tl);
       for (int kb = kb0; kb < kb1; ++kb) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait(tempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns);
@@ -507,7 +518,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         __syncwarp();
         const uint32_t dst = tbase + stage * G::kTStageBytes;
         if (lane < nbox)
-          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, (SPLIT ? kb : k_rot(p, tl, kb)) * kBKe,
+          tma_load_2d(dst + lane * (kTokBox * kBK * 2), &maps.tok, k_at(p, rot, kb) * kBKe,
                       tl.tok0 + lane * kTokBox,
                       tfull_bar(stage), tpol);
         pending |= 1u << stage;
