@@ -343,11 +343,11 @@ def quantize_activation_fp8(a, beta: float, beta_u: float) -> np.ndarray:
     return round_e4m3(np.asarray(a, np.float64) * np.float64(r)) * np.float64(s_h)
 
 
-def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weights_fp8, gamma, beta: float,
-                      beta_u: float, eps: float, norm: str = "expert") -> np.ndarray:
-    """routed_latent with fp8 experts: z (the bf16 values the layer stores) quantized per
-    token, expert weights given as (q, s) pairs per expert, h quantized with the fixed
-    scale, everything else in fp64.  `norm` places latent_norm as in routed_latent."""
+def _routed_latent_lowp(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, expert_mats, gamma, beta: float,
+                        beta_u: float, eps: float, norm: str) -> np.ndarray:
+    """The routed latent of the low-precision experts: z (the bf16 values the layer stores)
+    quantized per token to e4m3, expert_mats(e) -> (W_g, W_u, W_d) the dequantized weights of
+    expert e (fp64), h quantized with the fixed SiTU-GLU scale, everything else in fp64."""
     _check_norm(norm)
     z = np.asarray(z_bf16, np.float64)
     n, latent = z.shape
@@ -357,16 +357,30 @@ def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weight
     gamma = _f64(gamma)
     for e in np.unique(idx):
         rows, ks = np.nonzero(idx == e)
-        (gq, gs), (uq, us), (dq, ds) = weights_fp8[int(e)]
-        wg = gq * np.asarray(gs, np.float64)[:, None]
-        wu = uq * np.asarray(us, np.float64)[:, None]
-        wd = dq * np.asarray(ds, np.float64)[:, None]
+        wg, wu, wd = expert_mats(int(e))
         zr = zd[rows]
         a = situ_glu(zr @ wg.T, zr @ wu.T, beta, beta_u)
         y = quantize_activation_fp8(a, beta, beta_u) @ wd.T
         term = rms_norm(y, gamma, eps) if norm == "expert" else y
         c[rows] += _f64(w)[rows, ks][:, None] * term
     return rms_norm(c, gamma, eps) if norm == "combined" else c
+
+
+def routed_latent_fp8(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weights_fp8, gamma, beta: float,
+                      beta_u: float, eps: float, norm: str = "expert") -> np.ndarray:
+    """routed_latent with fp8 experts: z (the bf16 values the layer stores) quantized per
+    token, expert weights given as (q, s) pairs per expert, h quantized with the fixed
+    scale, everything else in fp64.  `norm` places latent_norm as in routed_latent."""
+    def mats(e):
+        return tuple(q * np.asarray(s, np.float64)[:, None] for q, s in weights_fp8[e])
+    return _routed_latent_lowp(z_bf16, idx, w, mats, gamma, beta, beta_u, eps, norm)
+
+
+def _layer_forward_lowp(x, idx, w, weights, routed, beta, beta_u, eps, z_bf16, norm):
+    x = _f64(x)
+    z = bf16_round((x @ _f64(weights["w_down"]).T).astype(np.float32)) if z_bf16 is None else _f64(z_bf16)
+    c = routed(z, idx, w, weights["latent_gamma"], beta, beta_u, eps, norm)
+    return c @ _f64(weights["w_up"]).T + shared_experts(x, weights, beta, beta_u)
 
 
 def layer_forward_fp8(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, weights_fp8, beta: float = 4.0,
@@ -378,10 +392,80 @@ def layer_forward_fp8(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, we
     (q, s) pairs of expert e's gate, up and down weights.  z_bf16, if given, is used as the
     stored z (the per-token scale is a discontinuous function of z, so parity checks take
     the same stored values on both sides, as routing takes the same logits)."""
-    x = _f64(x)
-    z = bf16_round((x @ _f64(weights["w_down"]).T).astype(np.float32)) if z_bf16 is None else _f64(z_bf16)
-    c = routed_latent_fp8(z, idx, w, weights_fp8, weights["latent_gamma"], beta, beta_u, eps, norm)
-    return c @ _f64(weights["w_up"]).T + shared_experts(x, weights, beta, beta_u)
+    def routed(z, idx_, w_, gamma, b, bu, ep, nm):
+        return routed_latent_fp8(z, idx_, w_, weights_fp8, gamma, b, bu, ep, nm)
+    return _layer_forward_lowp(x, idx, w, weights, routed, beta, beta_u, eps, z_bf16, norm)
+
+
+# --------------------------------------------------------------------------- MXFP4 experts
+#
+# [Sparse] ("Sparse by design") sizes the released model at about 1.4 TB of weights in MXFP4,
+# and [K3-news] ¶"第一" ties low-precision inference to the bounded SiTU-GLU.  The pages name the
+# format only.  Reading taken (the microscaling FP4 format as the OCP MX specification defines
+# it):
+#   * each routed-expert weight row is cut into blocks of 32 consecutive values along its input
+#     (K) axis; a block shares one power-of-two scale X = 2^x stored as an unsigned 8-bit
+#     exponent (x + 127), with x = floor(log2(max |w| of the block)) - 2 (2 is the largest
+#     exponent of an e2m1 value), clamped to [-127, 127]; an all-zero block takes x = -127;
+#   * each element is e2m1(w / X): the nearest of 0, 0.5, 1, 1.5, 2, 3, 4, 6 with the sign of w,
+#     on a tie the value whose mantissa bit is 0, saturating at +-6 (|w| / X < 8, so a block's
+#     largest element becomes 4 or 6);
+#   * the experts' token rows and their activation h are quantized as in the fp8 reading (e4m3
+#     per token; e4m3 with the fixed SiTU-GLU scale), so the MXFP4 layer differs from the fp8 one
+#     in the expert weights only.
+
+E2M1_MAX = 6.0
+MX_BLOCK = 32
+
+
+def round_e2m1(v) -> np.ndarray:
+    """Nearest e2m1 value (1 sign, 2 exponent bits with bias 1, 1 mantissa bit: magnitudes 0,
+    0.5, 1, 1.5, 2, 3, 4, 6), ties to the even mantissa, saturating at +-6."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), E2M1_MAX)
+    quantum = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))   # value spacing of each binade
+    q = np.round(a / quantum) * quantum                               # np.round: half to even
+    return np.where(a > 0, np.copysign(q, v), 0.0 * v)
+
+
+def quantize_rows_mxfp4(w) -> tuple[np.ndarray, np.ndarray]:
+    """MXFP4 quantization along the last axis (a multiple of 32): returns (q, x) with q the
+    e2m1 values (float64, the shape of w) and x the int32 block exponents [..., cols / 32], so
+    that w ~= q * 2^x blockwise (see the MXFP4 reading above)."""
+    w = np.asarray(w, np.float64)
+    cols = w.shape[-1]
+    assert cols % MX_BLOCK == 0
+    b = w.reshape(*w.shape[:-1], cols // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(b).max(axis=-1)
+    _, ex = np.frexp(amax)                       # amax = m 2^ex, m in [0.5, 1): floor(log2 amax) = ex - 1
+    x = np.where(amax > 0, ex - 1 - 2, -127)
+    x = np.clip(x, -127, 127).astype(np.int32)
+    q = round_e2m1(b / np.exp2(x.astype(np.float64))[..., None]).reshape(w.shape)
+    return q, x
+
+
+def dequantize_mxfp4(q, x) -> np.ndarray:
+    """q * 2^x with each block exponent applied to its 32 values."""
+    q = np.asarray(q, np.float64)
+    return q * np.repeat(np.exp2(np.asarray(x, np.float64)), MX_BLOCK, axis=-1)
+
+
+def routed_latent_mxfp4(z_bf16: np.ndarray, idx: np.ndarray, w: np.ndarray, weights_mx, gamma, beta: float,
+                        beta_u: float, eps: float, norm: str = "expert") -> np.ndarray:
+    """routed_latent with MXFP4 expert weights: weights_mx[e] holds the (q, x) pairs of expert
+    e's gate, up and down weights (quantize_rows_mxfp4); tokens and h as for the fp8 experts."""
+    def mats(e):
+        return tuple(dequantize_mxfp4(q, x) for q, x in weights_mx[e])
+    return _routed_latent_lowp(z_bf16, idx, w, mats, gamma, beta, beta_u, eps, norm)
+
+
+def layer_forward_mxfp4(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, weights_mx, beta: float = 4.0,
+                        beta_u: float = 25.0, eps: float = 1e-6, z_bf16: np.ndarray | None = None,
+                        norm: str = "expert") -> np.ndarray:
+    """Layer output with MXFP4 routed experts; otherwise as layer_forward_fp8 (z_bf16 as there)."""
+    def routed(z, idx_, w_, gamma, b, bu, ep, nm):
+        return routed_latent_mxfp4(z, idx_, w_, weights_mx, gamma, b, bu, ep, nm)
+    return _layer_forward_lowp(x, idx, w, weights, routed, beta, beta_u, eps, z_bf16, norm)
 
 
 def layer_forward(x: np.ndarray, idx: np.ndarray, w: np.ndarray, weights, beta: float = 4.0,

@@ -187,3 +187,52 @@ def test_fp8_activation_scale_from_gate_bound_only_is_caught(monkeypatch):
                         O.round_e4m3(np.asarray(a, np.float64) * (448.0 / beta)) * (beta / 448.0))
     assert _fails(P.test_fp8_activation_quantization_per_element)
     assert _fails(P.test_fp8_routed_latent_matches_brute_force)
+
+
+def test_mxfp4_scale_exponent_off_by_one_is_caught(monkeypatch):
+    # x = floor(log2 amax) - 1: the block maximum would map into [2, 4) instead of [4, 8)
+    orig = O.quantize_rows_mxfp4
+
+    def off(w):
+        q, x = orig(w)
+        x1 = np.minimum(x + 1, 127)
+        return O.round_e2m1(np.asarray(w, np.float64) / np.repeat(np.exp2(x1.astype(np.float64)), 32, axis=-1)), x1
+    monkeypatch.setattr(O, "quantize_rows_mxfp4", off)
+    assert _fails(P.test_quantize_rows_mxfp4_matches_per_block_brute_force)
+
+
+def test_mxfp4_per_row_scale_is_caught(monkeypatch):
+    # one scale per row (the largest block's) instead of one per block of 32
+    orig = O.quantize_rows_mxfp4
+
+    def per_row(w):
+        w = np.asarray(w, np.float64)
+        q, x = orig(w)
+        xr = np.repeat(x.max(axis=-1, keepdims=True), x.shape[-1], axis=-1)
+        return O.round_e2m1(w / np.repeat(np.exp2(xr.astype(np.float64)), 32, axis=-1)), xr
+    monkeypatch.setattr(O, "quantize_rows_mxfp4", per_row)
+    assert _fails(P.test_quantize_rows_mxfp4_matches_per_block_brute_force)
+
+
+def test_e2m1_ties_away_from_zero_is_caught(monkeypatch):
+    def half_away(v):
+        v = np.asarray(v, np.float64)
+        a = np.minimum(np.abs(v), 6.0)
+        qn = np.where(a < 2.0, 0.5, np.where(a < 4.0, 1.0, 2.0))
+        return np.copysign(np.floor(a / qn + 0.5) * qn, v)
+    monkeypatch.setattr(O, "round_e2m1", half_away)
+    assert _fails(P.test_round_e2m1_matches_table_search)
+
+
+def test_mxfp4_dropped_block_scale_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "dequantize_mxfp4", lambda q, x: np.asarray(q, np.float64))
+    assert _fails(P.test_dequantize_mxfp4_per_element)
+    assert _fails(P.test_mxfp4_routed_latent_matches_brute_force)
+
+
+def test_mxfp4_block_scales_tiled_instead_of_repeated_is_caught(monkeypatch):
+    # block exponents laid out b0 b1 b0 b1 ... along the row instead of 32 x b0, 32 x b1, ...
+    monkeypatch.setattr(O, "dequantize_mxfp4", lambda q, x: np.asarray(q, np.float64) *
+                        np.tile(np.exp2(np.asarray(x, np.float64)), 32))
+    assert _fails(P.test_dequantize_mxfp4_per_element)
+    assert _fails(P.test_mxfp4_routed_latent_matches_brute_force)

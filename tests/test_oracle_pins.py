@@ -725,3 +725,145 @@ def test_fp8_routed_latent_matches_brute_force():
     got = O.routed_latent_fp8(z, idx, w, wq, gamma, 4.0, 25.0, 1e-6)
     ref = _brute_fp8_routed_latent(z, idx, w, wq, gamma, 4.0, 25.0, 1e-6)
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------- MXFP4 experts
+
+def _e2m1_decode(code: int) -> float:
+    """Value of a 4-bit e2m1 code from its bit fields (sign bit 3, exponent bits 2-1 with bias 1,
+    mantissa bit 0; exponent 0 is subnormal: m * 0.5)."""
+    s, e, m = (code >> 3) & 1, (code >> 1) & 3, code & 1
+    mag = m * 0.5 if e == 0 else 2.0 ** (e - 1) * (1 + m / 2)
+    return -mag if s else mag
+
+
+def _e2m1_nearest(v: float) -> float:
+    """Nearest e2m1 value by search over the 16 decoded codes: the closer one, on an exact tie
+    the one with mantissa bit 0, +-6 beyond the range."""
+    table = sorted({(_e2m1_decode(c), c) for c in range(16) if c != 8})
+    if v >= 6.0:
+        return 6.0
+    if v <= -6.0:
+        return -6.0
+    best = None
+    for val, code in table:
+        d = abs(val - v)
+        if best is None or d < best[0] or (d == best[0] and (code & 1) == 0 and (best[2] & 1) == 1):
+            best = (d, val, code)
+    return best[1]
+
+
+def test_e2m1_codes_decode_to_the_eight_magnitudes():
+    mags = sorted({abs(_e2m1_decode(c)) for c in range(16)})
+    assert mags == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    for c in range(16):
+        assert O.round_e2m1(_e2m1_decode(c)) == _e2m1_decode(c)
+
+
+def test_round_e2m1_matches_table_search():
+    """e2m1 rounding against the nearest-code search, on random values over the whole range,
+    every midpoint between neighbouring values (the ties), the binade edges and values past
+    saturation, with both signs."""
+    rng = np.random.default_rng(31)
+    vals = list(rng.uniform(-8, 8, 3000)) + list(rng.normal(size=500) * 0.3)
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    mids = [(a + b) / 2 for a, b in zip(grid, grid[1:])]
+    vals += mids + [-m for m in mids] + grid + [6.5, 7.0, 1e9, -1e9, 2 - 1e-12, 4 - 1e-12, 1e-300]
+    got = O.round_e2m1(np.array(vals))
+    for v, g in zip(vals, got):
+        assert g == _e2m1_nearest(v), (v, g)
+    # ties go to the even mantissa: 0.25 -> 0, 0.75 -> 1, 1.25 -> 1, 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4
+    np.testing.assert_array_equal(O.round_e2m1(mids), [0.0, 1.0, 1.0, 2.0, 2.0, 4.0, 4.0])
+
+
+def test_quantize_rows_mxfp4_matches_per_block_brute_force():
+    """Per block of 32 along a row: the exponent is the one integer x with 4 <= amax / 2^x < 8
+    (found by search, clamped to [-127, 127]; an all-zero block takes -127), every element is the
+    nearest e2m1 code of w / 2^x, and the block's largest element lands on 4 or 6."""
+    rng = np.random.default_rng(32)
+    w = rng.normal(size=(6, 128)) * (10.0 ** rng.integers(-3, 3, size=(6, 1)))
+    w[1, 32:64] = 0.0                       # an all-zero block
+    w[2, :32] = 2.0 ** -140                 # below the smallest scale: the exponent clamps at -127
+    w[3, 64] = 6.0 * 2.0 ** 5               # a block whose maximum is exactly representable
+    w = O.bf16_round(w.astype(np.float32)).reshape(6, 128)
+    w[2, :32] = 2.0 ** -140
+    q, x = O.quantize_rows_mxfp4(w)
+    assert q.shape == w.shape and x.shape == (6, 4)
+    for r in range(6):
+        for b in range(4):
+            blk = w[r, 32 * b:32 * b + 32]
+            amax = max(abs(v) for v in blk)
+            if amax == 0:
+                want = -127
+            else:
+                want = next(e for e in range(-200, 200) if 4 <= amax / 2.0 ** e < 8)
+                want = max(-127, min(127, want))
+            assert x[r, b] == want, (r, b, x[r, b], want)
+            for i in range(32):
+                assert q[r, 32 * b + i] == _e2m1_nearest(blk[i] / 2.0 ** want), (r, b, i)
+            if amax > 0 and want > -127:
+                assert max(abs(v) for v in q[r, 32 * b:32 * b + 32]) in (4.0, 6.0)
+    assert np.all(q[1, 32:64] == 0) and np.all(q[2, :32] == 0)
+    np.testing.assert_array_equal(O.dequantize_mxfp4(q, x)[3, 64:65], [6.0 * 2.0 ** 5])
+
+
+def test_dequantize_mxfp4_per_element():
+    rng = np.random.default_rng(33)
+    q = O.round_e2m1(rng.uniform(-6, 6, size=(3, 96)))
+    x = rng.integers(-10, 10, size=(3, 3)).astype(np.int32)
+    got = O.dequantize_mxfp4(q, x)
+    for r in range(3):
+        for c in range(96):
+            assert got[r, c] == q[r, c] * 2.0 ** int(x[r, c // 32])
+
+
+def _mx_mats(qx):
+    """Dequantized weights of an MXFP4 (q, x) pair by a per-element loop."""
+    q, x = qx
+    return [[float(q[i][c]) * 2.0 ** int(x[i][c // 32]) for c in range(q.shape[1])] for i in range(q.shape[0])]
+
+
+def test_mxfp4_routed_latent_matches_brute_force():
+    """routed_latent_mxfp4 against the per-element loops of the fp8 brute force, fed the
+    block-dequantized weights (a per-element loop): tokens e4m3 per token, h with the fixed
+    SiTU-GLU scale, per-expert RMSNorm, weighted sum in k order."""
+    rng = np.random.default_rng(34)
+    bt, latent, inter, E, K = 4, 64, 32, 3, 2
+    z = O.bf16_round((rng.normal(size=(bt, latent)) * 2).astype(np.float32))
+    wmx, wq = {}, {}
+    for e in range(E):
+        g = rng.normal(size=(inter, latent)) * 0.5
+        g[:, :32] *= 8.0                     # blocks of one row at different scales
+        u = rng.normal(size=(inter, latent)) * 1.5
+        dn = rng.normal(size=(latent, inter)) * 0.3
+        wmx[e] = (O.quantize_rows_mxfp4(g), O.quantize_rows_mxfp4(u), O.quantize_rows_mxfp4(dn))
+        # the fp8 brute force takes (q, s) pairs: unit row scales on the dequantized matrices
+        wq[e] = tuple((np.array(_mx_mats(p)), np.ones(p[0].shape[0])) for p in wmx[e])
+    idx = np.array([[0, 2], [1, 0], [2, 1], [0, 1]], np.int32)
+    w = np.array([[0.7, 0.3], [0.5, 0.5], [0.9, 0.1], [0.25, 0.75]])
+    gamma = 1 + 0.1 * rng.normal(size=latent)
+    got = O.routed_latent_mxfp4(z, idx, w, wmx, gamma, 4.0, 25.0, 1e-6)
+    ref = _brute_fp8_routed_latent(z, idx, w, wq, gamma, 4.0, 25.0, 1e-6)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_mxfp4_routed_latent_is_close_to_bf16_one():
+    """MXFP4 weights move the routed latent by their rounding only: more than the e4m3 experts
+    (one mantissa bit instead of three) but within a bounded band of the unquantized path."""
+    w = WORKLOADS["small_bf16"]
+    s = w.shape
+    x, weights, _ = make_inputs(w, "cpu", 48)
+    W = _weights_np(weights)
+    z = O.bf16_round((_np(x) @ W["w_down"].T).astype(np.float32))
+    r = O.route(O.router_logits(_np(x), W["w_router"]), s.top_k)
+    ref = O.routed_latent(z, r["idx"], r["w"], W, s.beta, s.beta_u, s.rms_eps)
+    used = np.unique(r["idx"])
+    mx = {int(e): (O.quantize_rows_mxfp4(W["exp_gate"][e]), O.quantize_rows_mxfp4(W["exp_up"][e]),
+                   O.quantize_rows_mxfp4(W["exp_down"][e])) for e in used}
+    fp8 = {int(e): (O.quantize_rows_e4m3(W["exp_gate"][e]), O.quantize_rows_e4m3(W["exp_up"][e]),
+                    O.quantize_rows_e4m3(W["exp_down"][e])) for e in used}
+    got = O.routed_latent_mxfp4(z, r["idx"], r["w"], mx, W["latent_gamma"], s.beta, s.beta_u, s.rms_eps)
+    got8 = O.routed_latent_fp8(z, r["idx"], r["w"], fp8, W["latent_gamma"], s.beta, s.beta_u, s.rms_eps)
+    rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
+    rel8 = np.linalg.norm(got8 - ref) / np.linalg.norm(ref)
+    assert rel8 < rel < 0.3, (rel, rel8)
