@@ -37,31 +37,34 @@ METRIC = "LatentMoE layer fwd tokens/s on 1 B300; % of bf16 TC peak (or HBM BW)"
 
 # ----------------------------------------------------------------------------- arithmetic
 
-def algorithmic(shape, bt, n_touched, fp8_experts=False):
+def algorithmic(shape, bt, n_touched, fp8_experts=False, mxfp4_experts=False):
     """Algorithmic FLOPs and bytes of one layer call and of each stage (2*M*N*K per GEMM;
     bytes = what each stage must read and write at least once).  n_touched = experts
     with at least one token.  For the routed-expert GEMMs the bytes are the touched experts'
     weights only, the per-expert unit of the layer's byte count: their token rows and
     activations are intermediates of the layer (implementation traffic, which the measured
     DRAM traffic shows on top).  With fp8 experts the weights are one byte per value plus
-    4-byte row scales."""
+    4-byte row scales; with MXFP4 experts half a byte per value plus one scale byte per 32
+    values (17/32 byte per value)."""
     d, L, E, K, I, S, Is = (shape.d, shape.latent, shape.n_experts, shape.top_k, shape.expert_inter,
                             shape.n_shared, shape.shared_inter)
     b = 2 if shape.dtype == "bf16" else 4
-    if fp8_experts:
+    if fp8_experts or mxfp4_experts:
+        # per value, per output row
+        ev, er = (17 / 32, 0) if mxfp4_experts else (1, 4)
         st = {
             "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
             "cutoff_topk_segments": (0, 2 * bt * E * 4 + bt * K * 16),
             "w_down_gemm": (2 * bt * L * d, (bt * d + L * d + bt * L) * b),
             "token_gather": (0, bt * L * b + 2 * bt * L + bt * K * L),
-            "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, n_touched * 2 * I * (L + 4)),
-            "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * (I + 4)),
+            "expert_gate_up_gemm": (2 * bt * K * 2 * I * L, n_touched * 2 * I * (L * ev + er)),
+            "expert_down_gemm": (2 * bt * K * L * I, n_touched * L * (I * ev + er)),
             "rmsnorm_combine": (0, (bt * K * L + bt * L) * b + bt * K * 8),
             "shared_gate_up_gemm": (2 * bt * S * 2 * Is * d, (S * 2 * Is * d + bt * d + bt * S * Is) * b),
             "up_shared_down_gemm": (2 * bt * d * (L + S * Is), (d * (L + S * Is) + bt * (L + S * Is) + bt * d) * b),
         }
         flops = 2 * bt * (E * d + L * d + K * 3 * L * I + d * L + S * 3 * d * Is)
-        weight_bytes = (E * d + 2 * L * d + L + S * 3 * d * Is) * b + n_touched * 3 * L * I + n_touched * (2 * I + L) * 4
+        weight_bytes = (E * d + 2 * L * d + L + S * 3 * d * Is) * b + n_touched * 3 * L * I * ev + n_touched * (2 * I + L) * er
         return flops, weight_bytes + 2 * bt * d * b, st
     st = {
         "router_gemm": (2 * bt * E * d, (bt * d + E * d) * b + 2 * bt * E * 4),
@@ -409,11 +412,11 @@ def routing_stats(layer, xs):
     return sum(touched) / len(touched), max(load_max), min(load_min)
 
 
-def layer_fractions(shape, bt, n_touched, step_s, pk, fp8_experts=False):
+def layer_fractions(shape, bt, n_touched, step_s, pk, fp8_experts=False, mxfp4_experts=False):
     """The layer's achieved TFLOP/s and GB/s and their fractions of the measured bf16 tensor and
     HBM peaks; `bound` is the roof that binds (the larger of the two ideal times) and `frac`
     the fraction of that roof."""
-    flops, layer_bytes, _ = algorithmic(shape, bt, n_touched, fp8_experts=fp8_experts)
+    flops, layer_bytes, _ = algorithmic(shape, bt, n_touched, fp8_experts=fp8_experts, mxfp4_experts=mxfp4_experts)
     tc_frac = flops / step_s / 1e12 / pk["tc"]
     hbm_frac = layer_bytes / step_s / 1e9 / pk["hbm"]
     bound = "tensor" if flops / (pk["tc"] * 1e12) > layer_bytes / (pk["hbm"] * 1e9) else "hbm"
@@ -467,6 +470,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=None, help="default: --steps")
     ap.add_argument("--fp8-experts", action="store_true",
                     help="routed experts in e4m3 (lmoe_create_fp8); a separate line, not the bf16 headline")
+    ap.add_argument("--mxfp4-experts", action="store_true",
+                    help="routed experts in MXFP4 (lmoe_create_mxfp4); a separate line, not the bf16 headline")
     ap.add_argument("--bt", type=int, default=None,
                     help="tokens per step instead of the workload's (same shape and recipe); a separate line")
     ap.add_argument("--latent-norm", default="expert", choices=["expert", "combined"],
@@ -478,6 +483,9 @@ def main(argv=None):
         args.e2e_steps = args.steps
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.fp8_experts and args.mxfp4_experts:
+        ap.error("--fp8-experts and --mxfp4-experts are exclusive")
+    lowp = args.fp8_experts or args.mxfp4_experts
     ws, rank, local = dist_setup()
     if args.workload in FFN_WORKLOADS:
         return run_ffn(args, ws, rank, local)
@@ -506,6 +514,13 @@ def main(argv=None):
             del weights[n]
         torch.cuda.empty_cache()
         layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias, fp8_experts=f8)
+    elif args.mxfp4_experts:
+        from sparse_moe_layer_cutoff_b300.lmoe import quantize_experts_mxfp4
+        mx = quantize_experts_mxfp4(weights)
+        for n in ("exp_gate", "exp_up", "exp_down"):
+            del weights[n]
+        torch.cuda.empty_cache()
+        layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias, mxfp4_experts=mx)
     else:
         layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=bias)
     if args.latent_norm != "expert":
@@ -521,15 +536,16 @@ def main(argv=None):
 
     # ---- roofline of the dominant kernel (largest share of the timed region)
     pk = peaks()
-    flops, layer_bytes, per_stage = algorithmic(s, w.bt, n_touched, fp8_experts=args.fp8_experts)
+    flops, layer_bytes, per_stage = algorithmic(s, w.bt, n_touched, fp8_experts=args.fp8_experts,
+                                                mxfp4_experts=args.mxfp4_experts)
     dom = max(stage_ms, key=lambda k: stage_ms[k])
     dom_ms = stage_ms[dom] / max(calls, 1)
     f, b = per_stage[dom]
     long_step = ms / 1e3 > 2.0
     tc_peak = pk["tc_sustained"] if long_step else pk["tc"]
-    # the e4m3 expert GEMMs take the fp8 peak: the measured bf16 peak x the nominal fp8 / bf16
-    # dense ratio (4.5 / 2.25 PFLOP/s)
-    f8_kernel = args.fp8_experts and dom in ("expert_gate_up_gemm", "expert_down_gemm")
+    # the e4m3 (and e2m1 x e4m3) expert GEMMs take the fp8 peak: the measured bf16 peak x the
+    # nominal fp8 / bf16 dense ratio (4.5 / 2.25 PFLOP/s)
+    f8_kernel = lowp and dom in ("expert_gate_up_gemm", "expert_down_gemm")
     if f8_kernel:
         tc_peak *= 2.0
     if f / (tc_peak * 1e12) > b / (pk["hbm"] * 1e9):
@@ -543,7 +559,8 @@ def main(argv=None):
                                                 " burst" if roof["bound"] == "tensor" else "")
                  + (" bf16 x 2 (nominal fp8 / bf16 ratio)" if (roof["bound"] == "tensor" and f8_kernel) else "")})
     step_s = ms / 1e3 / args.steps
-    layer_roof = layer_fractions(s, w.bt, n_touched, step_s, pk, fp8_experts=args.fp8_experts)
+    layer_roof = layer_fractions(s, w.bt, n_touched, step_s, pk, fp8_experts=args.fp8_experts,
+                                 mxfp4_experts=args.mxfp4_experts)
     layer_roof["expert_load"] = {"max": load_max, "min": load_min, "target": w.bt * s.top_k / s.n_experts}
 
     # ---- end to end through the C ABI host-buffer call (lmoe_forward_host): every step copies
@@ -572,14 +589,14 @@ def main(argv=None):
 
     # ---- CPU oracle baseline (rank 0, one GPU only)
     cpu = None
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not args.fp8_experts and args.latent_norm == "expert":
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline and not lowp and args.latent_norm == "expert":
         t = oracle_sample_time(w, x, weights, bias, args.cpu_tokens)
         cpu = {"value": args.cpu_tokens / t, "unit": "tokens/s", "cores": _blas_threads(), "kind": "oracle",
                "sample": f"{args.cpu_tokens} tokens spread over the batch, routed among themselves, "
                          f"{t:.1f} s wall; expert weights fetched from HBM and upcast to fp64 inside the timing"}
 
     extras = {}
-    default_line = (args.workload == DEFAULT_WORKLOAD and args.bt is None and not args.fp8_experts and
+    default_line = (args.workload == DEFAULT_WORKLOAD and args.bt is None and not lowp and
                     args.latent_norm == "expert" and not args.no_extra)
     if default_line:
         layer.close()
@@ -608,6 +625,9 @@ def main(argv=None):
         if args.fp8_experts:
             line["dtype"] = "bf16 (routed experts e4m3)"
             line["metric"] = METRIC + " [fp8 routed experts]"
+        if args.mxfp4_experts:
+            line["dtype"] = "bf16 (routed experts e2m1 x e4m3, ue8m0 block scales)"
+            line["metric"] = METRIC + " [MXFP4 routed experts]"
         if args.latent_norm != "expert":
             line["metric"] += f" [latent norm: {args.latent_norm}]"
             line["config"]["latent_norm"] = args.latent_norm

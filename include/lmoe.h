@@ -316,6 +316,51 @@ LMOE_API lmoe_status lmoe_quantize_fp8_rows(const void* w, int64_t rows, int32_t
                                             lmoe_stream stream);
 
 /* ---------------------------------------------------------------------------------------
+ * MXFP4 routed experts ("Sparse by design", bittide.aicompass.dev translation of
+ * akashbajwa.co: the released model's weights are about 1.4 TB in MXFP4;
+ * "KimiK3的StableLatentMoE架构解析", ¶"第一": the bounded SiTU-GLU makes low-precision
+ * inference safe).  The format is the OCP microscaling FP4 one: each weight row is cut into
+ * blocks of 32 values along its input axis; a block shares a power-of-two scale 2^x stored as
+ * the byte x + 127 (ue8m0), x = floor(log2(max |w| of the block)) - 2 clamped to [-127, 127]
+ * (-127 for an all-zero block); each value is e2m1(w / 2^x) (magnitudes 0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6; nearest, ties to the even mantissa, saturating at 6).  The experts' input z and their
+ * activation are e4m3 as for lmoe_create_fp8; router, W_down, W_up and the shared experts stay
+ * bf16.  The expert GEMMs run as tcgen05 kind::mxf8f6f4 with block scaling (e2m1 weights x
+ * e4m3 tokens -> fp32).
+ *
+ * Layouts (both written by lmoe_quantize_mxfp4_rows):
+ *   codes: [rows, cols / 2] bytes, value 2j of a row in the low nibble of byte j, 2j + 1 in the
+ *          high nibble;
+ *   scales: tiled in 512-byte groups, one per (128-row block rb, 128-column block kb) at byte
+ *          (rb * (cols / 128) + kb) * 512; inside it, the scale of row r (r % 128 = 32 i + l)
+ *          for the 32 columns kb * 128 + 32 j ... + 31 is at byte 16 l + 4 i + j.
+ * Expert tensors [E, R, C] are E * R rows of C.
+ * --------------------------------------------------------------------------------------- */
+typedef struct {
+  const void* exp_gate;      /* e2m1 codes [E, I, L / 2] bytes (32-byte aligned)             */
+  const void* exp_up;        /* e2m1 codes [E, I, L / 2]                                     */
+  const void* exp_down;      /* e2m1 codes [E, L, I / 2]                                     */
+  const void* gate_sf;       /* ue8m0 block scales of exp_gate, E * I * L / 32 bytes, tiled  */
+  const void* up_sf;         /*                    of exp_up                                 */
+  const void* down_sf;       /*                    of exp_down, E * L * I / 32 bytes         */
+} lmoe_mxfp4_experts;
+
+/* As lmoe_create_fp8, with MXFP4 routed experts (borrowed device buffers, as produced by
+ * lmoe_quantize_mxfp4_rows; codes 32-byte and scales 16-byte aligned).  latent and
+ * expert_inter must be multiples of 128 (else LMOE_ERR_UNSUPPORTED).  In lmoe_workspace's
+ * view, h holds the e4m3 activations (bytes). */
+LMOE_API lmoe_status lmoe_create_mxfp4(const lmoe_config* cfg, const lmoe_weights* w,
+                                       const lmoe_mxfp4_experts* experts, int32_t max_bt, lmoe_stream stream,
+                                       lmoe_ctx** out);
+
+/* MXFP4 quantization as described above: w [rows, cols] bf16 (device, 16-byte aligned) ->
+ * codes [rows, cols / 2] bytes (16-byte aligned) and the tiled scales (rows * cols / 32 bytes),
+ * on `stream`.  rows == 0 does nothing; negative sizes or NULL / misaligned pointers give
+ * LMOE_ERR_INVALID_ARG; rows or cols not a multiple of 128 LMOE_ERR_UNSUPPORTED. */
+LMOE_API lmoe_status lmoe_quantize_mxfp4_rows(const void* w, int64_t rows, int32_t cols, void* q, void* sf,
+                                              lmoe_stream stream);
+
+/* ---------------------------------------------------------------------------------------
  * Dense SiTU-GLU FFN: the full-width feed-forward block of the model's first (dense) layer
  * ("Vue d'ensemble de l'architecture", mkdocs.reaper.mx, table "Le budget de paramètres,
  * module par module": 727 M parameters, intermediate 33 792 at d = 7168), with the experts'

@@ -1,7 +1,9 @@
 // Tensor-core engine of the layer: one persistent, warp-specialised tcgen05 GEMM kernel
 // serves every contraction ("Stable LatentMoE": router, down_proj, GroupedExperts gate/up +
 // SiTU-GLU, expert down, shared experts, up_proj + shared down), and the dense first-layer
-// FFN.  Operands are bf16 (kind::f16), or e4m3 for the fp8 routed experts (kind::f8f6f4).
+// FFN.  Operands are bf16 (kind::f16), e4m3 for the fp8 routed experts (kind::f8f6f4), or
+// MXFP4 weights against e4m3 tokens for the MXFP4 routed experts (kind::mxf8f6f4 with block
+// scaling: the weights' ue8m0 block scales go to TMEM by tcgen05.cp before each stage's MMAs).
 //
 // Weight-stationary tiles.  A tile is 256 weight rows (two MMA operands A0, A1 of M = 128
 // rows each) against up to kTokMax tokens (the MMA's N side, shared by both MMAs), with K
@@ -58,6 +60,13 @@ constexpr int kPartRows = 2 * kHalf;            // split-K partials: weight rows
 constexpr int kPartItem = kPartRows * 256;       // fp32 values per work item ([token][row], <= 256 tokens)
 constexpr int kSplitMinKb = 4;                   // k-blocks per split at least
 static_assert(kPartItem == kTcPartPerSm, "one work item of partials per SM at most");
+constexpr int kMxSfBytes = 512;                  // MXFP4: block scales of 128 rows x 128 K values
+// MXFP4 TMEM map: tiles of more than kMxNarrow tokens take both accumulator slots, so columns
+// [192, 256) and [448, 512) are never accumulators (tiles hold at most 192 tokens); the weight
+// stages' scales use 8 columns each from column 192, the tokens' unit scales 8 from 448.
+constexpr int kMxNarrow = 64;
+constexpr uint32_t kMxSfaCol = 192;
+constexpr uint32_t kMxSfbCol = 448;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
 
@@ -65,7 +74,7 @@ constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a tim
 // token tiles of up to 256 (more MMA work per k-block to cover the L2 round trip of their
 // operands) and need no expert schedule; grouped ones keep tiles of kTokMax tokens and the
 // schedule.
-template <bool DENSE>
+template <bool DENSE, bool MX = false>
 struct Geo {
   static constexpr int kTok = DENSE ? 256 : kTokMax;             // tokens per tile at most
   static constexpr int kWStages = 4;                             // weight ring (32 KB stages)
@@ -74,7 +83,10 @@ struct Geo {
   static constexpr int kTStageBytes = kTok * kBK * 2;            // token rows per stage
   static constexpr int kChunks = (kTok / 32 + 2) / 3;           // 32-token chunks per epilogue warp
   static constexpr int kOffT = kWStages * kWStageBytes;
-  static constexpr int kOffSched = kOffT + kTStages * kTStageBytes;
+  // MXFP4: the weight stages' block scales (512 bytes per operand) and the tokens' unit scales
+  static constexpr int kOffSf = kOffT + kTStages * kTStageBytes;
+  static constexpr int kOffSfUnit = kOffSf + (MX ? kWStages * 2 * kMxSfBytes : 0);
+  static constexpr int kOffSched = kOffSfUnit + (MX ? kMxSfBytes : 0);
   static constexpr int kOffBars = kOffSched + (DENSE ? 0 : 2 * kSchedMax * 4);
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
@@ -118,6 +130,8 @@ struct TcParams {
   const float* wscale_up;
   const float* tscale;      // per token (fp8 experts)
   const int32_t* perm;      // routed experts: slot -> token (token scales of the fp8 experts)
+  const uint8_t* sf0;       // MXFP4: tiled block scales of the weights (GLU: gate)
+  const uint8_t* sf1;       // MXFP4, GLU: up
   float h_mul, out_mul;
   unsigned long long timeout_ns;  // limit of every mbarrier wait
   int inject;               // test hook: the token producer leaves its stages unfilled
@@ -187,6 +201,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
+// 1-D bulk copy global -> shared memory (16-byte aligned, size a multiple of 16), completing on an
+// mbarrier, with an L2 policy.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
 // L2 policies: weights are streamed once (evict first); token rows are re-read by every
 // feature block of their tile (evict last).
 __device__ __forceinline__ uint64_t policy_evict_first() {
@@ -235,6 +257,22 @@ __device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
+// kind::mxf8f6f4 with block scaling: A = e2m1 weights (each 16-byte shared-memory chunk holds 16
+// values in its low 8 bytes), B = e4m3 tokens, 32 K-values per call; A's and B's scales are read
+// from TMEM at sfa / sfb, byte sf_id (set in idesc) of each 32-bit word.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc,
+                                          uint32_t sfa, uint32_t sfb) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc), "r"(sfa), "r"(sfb)
+      : "memory");
+}
+// 32 rows x 16 bytes of shared memory into 4 TMEM columns, the same 32 rows in each lane quadrant
+// (row l to lane l of every quadrant, its 4 words to the 4 columns).
+__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 template <bool F8>
 __device__ __forceinline__ void tc_mma_k(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
   if (F8) tc_mma_f8(d, a, b, idesc, acc);
@@ -247,6 +285,11 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// Shared-memory descriptor of a 32-row x 16-byte scale block: no swizzle, 8-row groups 128 bytes
+// apart (one 16-byte column, so no leading-dimension offset).
+__device__ __forceinline__ uint64_t sf_desc(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+}
 // Instruction descriptor: fp32 accumulator, A and B K-major; A / B format 1 = bf16 under
 // kind::f16, 0 = e4m3 under kind::f8f6f4.
 __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
@@ -255,6 +298,13 @@ __device__ __forceinline__ uint32_t idesc_bf16(int m, int n) {
 __device__ __forceinline__ uint32_t idesc_e4m3(int m, int n) {
   return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
 }
+// Block-scaled descriptor (kind::mxf8f6f4): A format 5 = e2m1, B format 0 = e4m3, both K-major,
+// scale type ue8m0 (bit 23); the scale-factor ids of B (bits 4-5) and A (bits 29-30) are ORed in
+// per K step by mx_sf_id.
+__device__ __forceinline__ uint32_t idesc_mx(int m, int n) {
+  return (5u << 7) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24);
+}
+__device__ __forceinline__ uint32_t mx_sf_id(uint32_t j) { return (j << 4) | (j << 29); }
 
 // tanh by the MUFU hardware approximation (PTX tanh.approx.f32).
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -384,11 +434,13 @@ __device__ __forceinline__ uint32_t acc_col(bool wide, int slot, int h) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int EPI, bool F8, bool DENSE, bool SPLIT>
+template <int EPI, bool F8, bool DENSE, bool SPLIT, bool MX>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   static_assert(!SPLIT || (DENSE && !F8), "split-K covers the dense bf16 GEMMs");
-  using G = Geo<DENSE>;
+  static_assert(!MX || (F8 && !DENSE && !SPLIT && EPI != kEpiRouter), "MXFP4 covers the routed-expert GEMMs");
+  static_assert(kTokMax <= (int)kMxSfaCol, "MXFP4 scale columns lie past the widest accumulator");
+  using G = Geo<DENSE, MX>;
   constexpr int kBKe = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -396,6 +448,8 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   uint8_t* sbase = smem_raw + (base - raw);
   const uint32_t wbase = base;
   const uint32_t tbase = base + G::kOffT;
+  const uint32_t sfbase = base + G::kOffSf;        // MXFP4: block scales of each weight stage
+  const uint32_t sfunit = base + G::kOffSfUnit;    // MXFP4: the tokens' unit scales
   int32_t* s_seg = reinterpret_cast<int32_t*>(sbase + G::kOffSched);
   int32_t* s_mt = s_seg + kSchedMax;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sbase + G::kOffBars);
@@ -425,6 +479,12 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       s_seg[i] = p.seg_off[i];
       s_mt[i] = p.mtile_off[i];
     }
+  }
+  if (MX) {
+    // the token operand carries its per-token scale in the epilogue: its MMA scales are all 2^0
+    uint32_t* unit = reinterpret_cast<uint32_t*>(sbase + G::kOffSfUnit);
+    for (int i = threadIdx.x; i < kMxSfBytes / 4; i += blockDim.x) unit[i] = 0x7F7F7F7Fu;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -471,13 +531,21 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(wempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
           pending &= ~(1u << stage);
-          mbar_expect_tx(wfull_bar(stage), (uint32_t)(nh * kHalfBytes));
+          // MXFP4 boxes write their 8 KB of packed codes into the low halves of 16 KB of chunks
+          mbar_expect_tx(wfull_bar(stage), (uint32_t)(nh * (MX ? kHalfBytes / 2 + kMxSfBytes : kHalfBytes)));
           const uint32_t dst = wbase + stage * kWStageBytes;
+          const int kq = k_at(p, rot, kb);
           for (int h = 0; h < nh; ++h) {
             const CUtensorMap* m;
             int x, y;
-            w_src(tl, k_at(p, rot, kb), h, m, x, y);
+            w_src(tl, kq, h, m, x, y);
             tma_load_2d(dst + h * kHalfBytes, m, x, y, wfull_bar(stage), wpol);
+            if (MX) {
+              // the 512 scale bytes of these 128 weight rows x 128 K values
+              const uint8_t* sf = (EPI == kEpiGlu && h) ? p.sf1 : p.sf0;
+              bulk_load(sfbase + (uint32_t)(stage * 2 + h) * kMxSfBytes,
+                        sf + ((long long)(y >> 7) * p.kblocks + kq) * kMxSfBytes, kMxSfBytes, wfull_bar(stage), wpol);
+            }
           }
           pending |= 1u << stage;
           pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
@@ -538,13 +606,19 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       uint32_t wph = 0, tph = 0;
       uint32_t aph[2] = {0u, 0u};
       bool stop = false, issued = false;
+      if (MX) {
+        // unit scales of the token operand, 8 columns (up to 256 tokens)
+        tc_cp_sf(tmem_base + kMxSfbCol, sf_desc(sfunit));
+        tc_cp_sf(tmem_base + kMxSfbCol + 4u, sf_desc(sfunit));
+        issued = true;
+      }
       for (int t = blockIdx.x; t < nwork && !stop; t += gridDim.x) {
         int kb0, kb1;
         const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
         const int ntr = (tl.ntok + 15) & ~15;
-        const bool wide = ntr > kHalf;
+        const bool wide = ntr > (MX ? kMxNarrow : kHalf);
         const int nh = tile_halves<EPI>(p, tl);
-        const uint32_t idesc = F8 ? idesc_e4m3(kHalf, ntr) : idesc_bf16(kHalf, ntr);
+        const uint32_t idesc = MX ? idesc_mx(kHalf, ntr) : F8 ? idesc_e4m3(kHalf, ntr) : idesc_bf16(kHalf, ntr);
         if (wide) {
           if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status, p.timeout_ns) ||
               !mbar_wait(aempty_bar(1), aph[1] ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
@@ -560,14 +634,33 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           tc_fence_after();
           const uint64_t ad = smem_desc(wbase + ws * kWStageBytes);
           const uint64_t bd = smem_desc(tbase + ts * G::kTStageBytes);
-#pragma unroll
-          for (int j = 0; j < kBK / 16; ++j)
-            tc_mma_k<F8>(d0, ad + 2u * j, bd + 2u * j, idesc, (kb != kb0 || j != 0) ? 1u : 0u);
-          if (nh == 2) {
-            const uint64_t ad1 = ad + (uint64_t)(kHalfBytes >> 4);
+          if (MX) {
+            // this stage's weight scales into its TMEM columns (issued before, so ordered before,
+            // the MMAs that read them; the columns' previous MMAs completed before the stage refilled)
+            const uint32_t sfa = tmem_base + kMxSfaCol + 8u * ws;
+            tc_cp_sf(sfa, sf_desc(sfbase + (uint32_t)(ws * 2) * kMxSfBytes));
+            if (nh == 2) tc_cp_sf(sfa + 4u, sf_desc(sfbase + (uint32_t)(ws * 2 + 1) * kMxSfBytes));
 #pragma unroll
             for (int j = 0; j < kBK / 16; ++j)
-              tc_mma_k<F8>(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb != kb0 || j != 0) ? 1u : 0u);
+              tc_mma_mx(d0, ad + 2u * j, bd + 2u * j, idesc | mx_sf_id(j), (kb != kb0 || j != 0) ? 1u : 0u, sfa,
+                        tmem_base + kMxSfbCol);
+            if (nh == 2) {
+              const uint64_t ad1 = ad + (uint64_t)(kHalfBytes >> 4);
+#pragma unroll
+              for (int j = 0; j < kBK / 16; ++j)
+                tc_mma_mx(d1, ad1 + 2u * j, bd + 2u * j, idesc | mx_sf_id(j), (kb != kb0 || j != 0) ? 1u : 0u, sfa + 4u,
+                          tmem_base + kMxSfbCol);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j)
+              tc_mma_k<F8>(d0, ad + 2u * j, bd + 2u * j, idesc, (kb != kb0 || j != 0) ? 1u : 0u);
+            if (nh == 2) {
+              const uint64_t ad1 = ad + (uint64_t)(kHalfBytes >> 4);
+#pragma unroll
+              for (int j = 0; j < kBK / 16; ++j)
+                tc_mma_k<F8>(d1, ad1 + 2u * j, bd + 2u * j, idesc, (kb != kb0 || j != 0) ? 1u : 0u);
+            }
           }
           issued = true;
           tc_commit(wempty_bar(ws));
@@ -604,7 +697,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       int kb0, kb1;
       const Tile tl = decode_work<SPLIT>(p, seg, mt, t, kb0, kb1);
       const int ntr = (tl.ntok + 15) & ~15;
-      const bool wide = ntr > kHalf;
+      const bool wide = ntr > (MX ? kMxNarrow : kHalf);
       const int nh = tile_halves<EPI>(p, tl);
       bool ok;
       if (wide) ok = mbar_wait(afull_bar(0), aph[0], abort_flag, p.status, p.timeout_ns) &&
@@ -656,7 +749,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       } else if (EPI == kEpiGlu) {
         // fp8: per-row weight scales of this lane's feature (gate and up rows)
         float sg = 1.f, su = 1.f;
-        if (F8) {
+        if (F8 && !MX) {
           const int fo = tl.fb * kHalf + q * 32 + lane;
           if (fo < p.n_feat) {
             sg = p.wscale[(long long)tl.g * p.w_group_rows + fo];
@@ -713,7 +806,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                 float sc = 1.f;   // fp8: row scale times the activation scale
                 if (F8) {
                   const int fo = tl.fb * 2 * kHalf + h * kHalf + q * 32 + lane;
-                  if (fo < p.n_feat) sc = p.wscale[(long long)tl.g * p.w_group_rows + fo] * p.out_mul;
+                  if (fo < p.n_feat) sc = (MX ? 1.f : p.wscale[(long long)tl.g * p.w_group_rows + fo]) * p.out_mul;
                 }
                 tmem_wait_ld();
 #pragma unroll
@@ -886,6 +979,22 @@ bool make_map(CUtensorMap* m, const void* base, long long rows, long long cols, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D map over rows x cols e2m1 codes packed two per byte (row stride cols / 2 bytes): boxes of
+// 128 values (64 bytes) x box_rows rows, each 8-byte group of 16 values landing in the low half of
+// a 16-byte shared-memory chunk (16U4_ALIGN16B), 128-byte swizzle: the shared-memory image of a
+// box is that of a 128-column box of bytes.
+bool make_map_fp4(CUtensorMap* m, const void* base, long long rows, long long cols, int box_rows) {
+  EncodeTiledFn enc = encoder();
+  if (!enc || rows <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols / 2)};
+  cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Token tile of a dense GEMM: the multiple of 16 in [128, 256] that minimises
 // waves x (tile + a fixed per-tile cost of 32 tokens), so the last wave of the persistent
 // grid is nearly full (e.g. the 8192-token router: 172 tiles of 192 tokens leave most of
@@ -903,9 +1012,9 @@ int dense_tok_tile(int bt, int n_fb, int grid) {
   return best;
 }
 
-template <int EPI, bool F8, bool DENSE, bool SPLIT = false>
+template <int EPI, bool F8, bool DENSE, bool SPLIT = false, bool MX = false>
 cudaError_t launch_kernel(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t st) {
-  tc_gemm_kernel<EPI, F8, DENSE, SPLIT><<<grid, kThreads, Geo<DENSE>::kSmemBytes, st>>>(maps, p);
+  tc_gemm_kernel<EPI, F8, DENSE, SPLIT, MX><<<grid, kThreads, Geo<DENSE, MX>::kSmemBytes, st>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -926,7 +1035,8 @@ cudaError_t launch_split(const TcMaps& maps, const TcParams& p, int grid, int sm
 // items).  A dense GEMM with at most half as many tiles as SMs and a partial buffer
 // (p.part) is split along K into up to SMs / tiles work items per tile (each of at least
 // kSplitMinKb k-blocks) and reduced by a second kernel.  *n = kernels launched.
-cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st, bool f8, int* n) {
+cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st, bool f8, int* n,
+                      bool mx = false) {
   *n = 0;
   p.ksplit = 1;
   if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, sm_count);
@@ -942,6 +1052,10 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
   }
   if (grid <= 0) return cudaSuccess;
   *n = p.ksplit > 1 ? 2 : 1;
+  if (mx) {   // the MXFP4 routed experts (grouped)
+    if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false, false, true>(maps, p, grid, st);
+    return launch_kernel<kEpiStore, true, false, false, true>(maps, p, grid, st);
+  }
   if (f8) {   // the fp8 routed experts (grouped)
     if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false>(maps, p, grid, st);
     return launch_kernel<kEpiStore, true, false>(maps, p, grid, st);
@@ -964,14 +1078,14 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
   }
 }
 
-template <int EPI, bool F8, bool DENSE, bool SPLIT = false>
+template <int EPI, bool F8, bool DENSE, bool SPLIT = false, bool MX = false>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Geo<DENSE>::kSmemBytes);
+  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE, SPLIT, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Geo<DENSE, MX>::kSmemBytes);
 }
 
 // Raises the dynamic shared-memory limit of every kernel instance a plan launches.
-cudaError_t prepare_kernels(bool f8) {
+cudaError_t prepare_kernels(bool f8, bool mx = false) {
   cudaError_t e = set_smem<kEpiStore, false, true>();
   if (e == cudaSuccess) e = set_smem<kEpiGlu, false, true>();
   if (e == cudaSuccess) e = set_smem<kEpiRouter, false, true>();
@@ -982,6 +1096,8 @@ cudaError_t prepare_kernels(bool f8) {
   if (e == cudaSuccess) e = set_smem<kEpiGlu, false, false>();
   if (e == cudaSuccess && f8) e = set_smem<kEpiGlu, true, false>();
   if (e == cudaSuccess && f8) e = set_smem<kEpiStore, true, false>();
+  if (e == cudaSuccess && mx) e = set_smem<kEpiGlu, true, false, false, true>();
+  if (e == cudaSuccess && mx) e = set_smem<kEpiStore, true, false, false, true>();
   return e;
 }
 
@@ -992,17 +1108,19 @@ struct TcPlan {
   int max_bt;
   int sm_count;
   TcBuffers buf;
-  bool f8;                                                  // e4m3 routed experts
+  bool f8;                                                  // e4m3 token rows and h (fp8 or MXFP4 experts)
+  bool mx;                                                  // MXFP4 expert weights
   CUtensorMap m_gate8, m_up8, m_edown8, m_zq8, m_h8;        // their weights, token rows, h
-  const float *s_gate, *s_up, *s_down;                      // per-row weight scales
+  const float *s_gate, *s_up, *s_down;                      // fp8: per-row weight scales
+  const uint8_t *sf_gate, *sf_up, *sf_down;                 // MXFP4: tiled block scales
   float h_mul, h_scale;                                     // fixed activation scale (SiTU-GLU bound)
   bool inject;                                              // test hook armed for the next expert gate/up
   CUtensorMap m_router, m_down, m_gate, m_up, m_edown, m_shg, m_shu, m_wup, m_shd;  // weights
   CUtensorMap m_zp, m_h, m_cat;                                                       // workspace
 };
 
-lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int max_bt,
-                           int sm_count, const TcBuffers& buf, TcPlan** plan) {
+lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8,
+                           const lmoe_mxfp4_experts* mx, int max_bt, int sm_count, const TcBuffers& buf, TcPlan** plan) {
   *plan = nullptr;
   TcPlan* pl = new (std::nothrow) TcPlan();
   if (!pl) return LMOE_ERR_OOM;
@@ -1014,16 +1132,25 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const 
   const long long E = c.n_experts, d = c.d, L = c.latent, I = c.expert_inter, S = c.n_shared, Is = c.shared_inter;
   const long long ldc = L + S * Is;
   const long long slots = (long long)max_bt * c.top_k;
-  pl->f8 = f8 != nullptr;
+  pl->f8 = f8 != nullptr || mx != nullptr;
+  pl->mx = mx != nullptr;
   bool ok = make_map(&pl->m_router, w->w_router, E, d, d, kHalf) && make_map(&pl->m_down, w->w_down, L, d, d, kHalf);
   if (pl->f8) {
-    ok = ok && make_map(&pl->m_gate8, f8->exp_gate, E * I, L, L, kHalf, true) &&
-         make_map(&pl->m_up8, f8->exp_up, E * I, L, L, kHalf, true) &&
-         make_map(&pl->m_edown8, f8->exp_down, E * L, I, I, kHalf, true) &&
-         make_map(&pl->m_zq8, buf.zp, slots, L, L, kTokBox, true) && make_map(&pl->m_h8, buf.h, slots, I, I, kTokBox, true);
-    pl->s_gate = f8->gate_scale;
-    pl->s_up = f8->up_scale;
-    pl->s_down = f8->down_scale;
+    if (pl->mx) {
+      ok = ok && make_map_fp4(&pl->m_gate8, mx->exp_gate, E * I, L, kHalf) &&
+           make_map_fp4(&pl->m_up8, mx->exp_up, E * I, L, kHalf) && make_map_fp4(&pl->m_edown8, mx->exp_down, E * L, I, kHalf);
+      pl->sf_gate = static_cast<const uint8_t*>(mx->gate_sf);
+      pl->sf_up = static_cast<const uint8_t*>(mx->up_sf);
+      pl->sf_down = static_cast<const uint8_t*>(mx->down_sf);
+    } else {
+      ok = ok && make_map(&pl->m_gate8, f8->exp_gate, E * I, L, L, kHalf, true) &&
+           make_map(&pl->m_up8, f8->exp_up, E * I, L, L, kHalf, true) &&
+           make_map(&pl->m_edown8, f8->exp_down, E * L, I, I, kHalf, true);
+      pl->s_gate = f8->gate_scale;
+      pl->s_up = f8->up_scale;
+      pl->s_down = f8->down_scale;
+    }
+    ok = ok && make_map(&pl->m_zq8, buf.zp, slots, L, L, kTokBox, true) && make_map(&pl->m_h8, buf.h, slots, I, I, kTokBox, true);
     const float bound = c.beta * c.beta_u;   // |SiTU-GLU| < beta * beta_u
     pl->h_mul = 448.0f / bound;
     pl->h_scale = bound / 448.0f;
@@ -1040,7 +1167,7 @@ lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const 
     delete pl;
     return LMOE_ERR_CUDA;
   }
-  cudaError_t e = prepare_kernels(pl->f8);
+  cudaError_t e = prepare_kernels(pl->f8, pl->mx);
   if (e != cudaSuccess) {
     cudaGetLastError();
     delete pl;
@@ -1140,6 +1267,8 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* 
         maps.tok = pl->m_zq8;
         p.wscale = pl->s_gate;
         p.wscale_up = pl->s_up;
+        p.sf0 = pl->sf_gate;
+        p.sf1 = pl->sf_up;
         p.tscale = pl->buf.tscale;
         p.perm = a.a_rows;
         p.h_mul = pl->h_mul;
@@ -1161,6 +1290,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* 
         maps.w[0] = pl->m_edown8;
         maps.tok = pl->m_h8;
         p.wscale = pl->s_down;
+        p.sf0 = pl->sf_down;
         p.out_mul = pl->h_scale;
         p.kblocks = a.K / (2 * kBK);
         f8 = true;
@@ -1178,7 +1308,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* 
   }
   if (!ok) return cudaErrorInvalidValue;
   p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
-  return launch_tc(maps, p, epi, pl->sm_count, st, f8, n);
+  return launch_tc(maps, p, epi, pl->sm_count, st, f8, n, f8 && pl->mx);
 }
 
 // ------------------------------------------------------------------ dense SiTU-GLU FFN

@@ -24,8 +24,10 @@ struct TcBuffers {
 // engine does not cover this configuration.
 // f8 != nullptr: routed experts in e4m3 (w's expert pointers are not used); h then holds
 // e4m3 bytes.
-lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int max_bt,
-                           int sm_count, const TcBuffers& buf, TcPlan** plan);
+// mx != nullptr: routed experts in MXFP4 (e2m1 codes with tiled ue8m0 block scales), with e4m3
+// token rows and h as for f8.
+lmoe_status tc_plan_create(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8,
+                           const lmoe_mxfp4_experts* mx, int max_bt, int sm_count, const TcBuffers& buf, TcPlan** plan);
 void tc_plan_destroy(TcPlan* plan);
 // Test hook: the next routed-expert gate/up launch leaves its token stages unfilled and
 // shortens its waits to 20 ms, so the kernel times out, records LMOE timeout status and

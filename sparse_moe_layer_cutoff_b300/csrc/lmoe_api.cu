@@ -324,9 +324,10 @@ const char* lmoe_build_info(void) {
 
 namespace {
 
-// lmoe_create and lmoe_create_fp8 (f8 != nullptr: e4m3 routed experts).
-lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8, int32_t max_bt,
-                        lmoe_stream stream, lmoe_ctx** out) {
+// lmoe_create, lmoe_create_fp8 (f8 != nullptr: e4m3 routed experts) and lmoe_create_mxfp4
+// (mx != nullptr: MXFP4 routed experts; their tokens and h are e4m3 as with f8).
+lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* f8,
+                        const lmoe_mxfp4_experts* mx, int32_t max_bt, lmoe_stream stream, lmoe_ctx** out) {
   if (!out) return LMOE_ERR_INVALID_ARG;
   *out = nullptr;
   lmoe_status s = check_cfg(cfg);
@@ -334,9 +335,12 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   if (!w) return LMOE_ERR_INVALID_ARG;
   if (max_bt <= 0 || max_bt > (1 << 20)) return LMOE_ERR_INVALID_ARG;
   if ((long long)max_bt * cfg->top_k >= (1LL << 31)) return LMOE_ERR_UNSUPPORTED;
-  if (f8 && cfg->dtype != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
+  const bool lowp = f8 || mx;
+  if (lowp && cfg->dtype != LMOE_BF16) return LMOE_ERR_INVALID_ARG;
   const void* req[] = {w->w_router, w->w_down, w->latent_gamma, w->w_up, w->sh_gate, w->sh_up, w->sh_down,
-                       f8 ? f8->exp_gate : w->exp_gate, f8 ? f8->exp_up : w->exp_up, f8 ? f8->exp_down : w->exp_down};
+                       f8 ? f8->exp_gate : mx ? mx->exp_gate : w->exp_gate,
+                       f8 ? f8->exp_up : mx ? mx->exp_up : w->exp_up,
+                       f8 ? f8->exp_down : mx ? mx->exp_down : w->exp_down};
   for (const void* p : req)
     if (!p || !aligned16(p)) return LMOE_ERR_INVALID_ARG;
   if (w->router_bias && !aligned16(w->router_bias)) return LMOE_ERR_INVALID_ARG;
@@ -345,13 +349,25 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
     for (const float* p : sc)
       if (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) return LMOE_ERR_INVALID_ARG;
   }
+  if (mx) {
+    // TMA reads the packed codes from 32-byte aligned rows; the scale groups are bulk-copied
+    const void* codes[] = {mx->exp_gate, mx->exp_up, mx->exp_down};
+    for (const void* p : codes)
+      if (reinterpret_cast<uintptr_t>(p) & 31u) return LMOE_ERR_INVALID_ARG;
+    const void* sc[] = {mx->gate_sf, mx->up_sf, mx->down_sf};
+    for (const void* p : sc)
+      if (!p || !aligned16(p)) return LMOE_ERR_INVALID_ARG;
+    if (cfg->latent % 128 || cfg->expert_inter % 128) return LMOE_ERR_UNSUPPORTED;
+  }
   // from here on the CUDA runtime is needed
   for (const void* p : req)
     if ((s = check_device_ptr(p)) != LMOE_OK) return s;
   if (w->router_bias && (s = check_device_ptr(w->router_bias)) != LMOE_OK) return s;
-  if (f8) {
-    const void* sc[] = {f8->gate_scale, f8->up_scale, f8->down_scale};
-    for (const void* p : sc) {
+  if (lowp) {
+    const void* sc8[] = {f8 ? (const void*)f8->gate_scale : nullptr, f8 ? (const void*)f8->up_scale : nullptr,
+                         f8 ? (const void*)f8->down_scale : nullptr};
+    const void* scmx[] = {mx ? mx->gate_sf : nullptr, mx ? mx->up_sf : nullptr, mx ? mx->down_sf : nullptr};
+    for (const void* p : (f8 ? sc8 : scmx)) {
       cudaPointerAttributes at;
       if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
         cudaGetLastError();
@@ -368,7 +384,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->max_bt = max_bt;
   ctx->stream = static_cast<cudaStream_t>(stream);
   ctx->bf16 = cfg->dtype == LMOE_BF16;
-  ctx->f8 = f8 != nullptr;
+  ctx->f8 = lowp;
   ctx->esz = ctx->bf16 ? 2 : 4;
   const char* chk = getenv("LMOE_CHECK");
   ctx->check = chk && chk[0] == '1';
@@ -400,7 +416,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   size_t o_list = cv.take<int32_t>(bt + 1);
   size_t o_status = cv.take<uint32_t>(4);
   size_t o_z = cv.take<char>(bt * L * ctx->esz);
-  size_t o_zq = f8 ? cv.take<char>(bt * L) : 0;
+  size_t o_zq = lowp ? cv.take<char>(bt * L) : 0;
   size_t o_zp = ctx->bf16 ? cv.take<char>(bt * K * L * 2) : 0;
   size_t o_h = cv.take<char>(bt * K * c.expert_inter * ctx->esz);
   size_t o_y = cv.take<char>(bt * K * L * ctx->esz);
@@ -429,7 +445,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->topk_list = (int32_t*)(b + o_list);
   ctx->status = (uint32_t*)(b + o_status);
   ctx->z = b + o_z;
-  ctx->zq = f8 ? b + o_zq : nullptr;
+  ctx->zq = lowp ? b + o_zq : nullptr;
   ctx->zp = ctx->bf16 ? b + o_zp : nullptr;
   ctx->h = b + o_h;
   ctx->y = b + o_y;
@@ -446,7 +462,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
   ctx->tc = nullptr;
   if (ctx->bf16) {
     const char* force = getenv("LMOE_FORCE_SIMT");
-    if (f8 && force && force[0] == '1') {
+    if (lowp && force && force[0] == '1') {
       cudaFree(ctx->ws);
       delete ctx;
       return LMOE_ERR_UNSUPPORTED;
@@ -457,7 +473,7 @@ lmoe_status create_impl(const lmoe_config* cfg, const lmoe_weights* w, const lmo
       tb.tscale = ctx->tscale;
       tb.part = ctx->part;
       tb.status = ctx->status;
-      lmoe_status ts = tc_plan_create(&c, w, f8, max_bt, ctx->sm_count, tb, &ctx->tc);
+      lmoe_status ts = tc_plan_create(&c, w, f8, mx, max_bt, ctx->sm_count, tb, &ctx->tc);
       if (ts != LMOE_OK) {
         cudaFree(ctx->ws);
         delete ctx;
@@ -476,7 +492,7 @@ extern "C" {
 
 lmoe_status lmoe_create(const lmoe_config* cfg, const lmoe_weights* w, int32_t max_bt, lmoe_stream stream,
                         lmoe_ctx** out) {
-  return logged("lmoe_create", create_impl(cfg, w, nullptr, max_bt, stream, out));
+  return logged("lmoe_create", create_impl(cfg, w, nullptr, nullptr, max_bt, stream, out));
 }
 
 lmoe_status lmoe_create_fp8(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_fp8_experts* experts,
@@ -485,7 +501,16 @@ lmoe_status lmoe_create_fp8(const lmoe_config* cfg, const lmoe_weights* w, const
     if (out) *out = nullptr;
     return logged("lmoe_create_fp8", LMOE_ERR_INVALID_ARG);
   }
-  return logged("lmoe_create_fp8", create_impl(cfg, w, experts, max_bt, stream, out));
+  return logged("lmoe_create_fp8", create_impl(cfg, w, experts, nullptr, max_bt, stream, out));
+}
+
+lmoe_status lmoe_create_mxfp4(const lmoe_config* cfg, const lmoe_weights* w, const lmoe_mxfp4_experts* experts,
+                              int32_t max_bt, lmoe_stream stream, lmoe_ctx** out) {
+  if (!experts) {
+    if (out) *out = nullptr;
+    return logged("lmoe_create_mxfp4", LMOE_ERR_INVALID_ARG);
+  }
+  return logged("lmoe_create_mxfp4", create_impl(cfg, w, nullptr, experts, max_bt, stream, out));
 }
 
 static lmoe_status route_entry(lmoe_ctx* ctx, const void* x, int32_t bt, lmoe_stream stream,

@@ -39,6 +39,10 @@ class lmoe_fp8_experts(ctypes.Structure):
     _fields_ = [(n, c_vp) for n in ("exp_gate", "exp_up", "exp_down", "gate_scale", "up_scale", "down_scale")]
 
 
+class lmoe_mxfp4_experts(ctypes.Structure):
+    _fields_ = [(n, c_vp) for n in ("exp_gate", "exp_up", "exp_down", "gate_sf", "up_sf", "down_sf")]
+
+
 class lmoe_ffn_config(ctypes.Structure):
     _fields_ = [("d", c_i32), ("inter", c_i32), ("beta", c_f32), ("beta_u", c_f32)]
 
@@ -91,6 +95,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.lmoe_create_fp8.restype = c_i32
     lib.lmoe_quantize_fp8_rows.argtypes = [c_vp, ctypes.c_int64, c_i32, c_vp, c_vp, c_vp]
     lib.lmoe_quantize_fp8_rows.restype = c_i32
+    lib.lmoe_create_mxfp4.argtypes = [ctypes.POINTER(lmoe_config), ctypes.POINTER(lmoe_weights),
+                                      ctypes.POINTER(lmoe_mxfp4_experts), c_i32, c_vp, ctypes.POINTER(c_vp)]
+    lib.lmoe_create_mxfp4.restype = c_i32
+    lib.lmoe_quantize_mxfp4_rows.argtypes = [c_vp, ctypes.c_int64, c_i32, c_vp, c_vp, c_vp]
+    lib.lmoe_quantize_mxfp4_rows.restype = c_i32
     lib.lmoe_ffn_create.argtypes = [ctypes.POINTER(lmoe_ffn_config), c_vp, c_vp, c_vp, c_i32, ctypes.POINTER(c_vp)]
     lib.lmoe_ffn_create.restype = c_i32
     lib.lmoe_ffn_forward.argtypes = [c_vp, c_vp, c_i32, c_vp, c_vp]
@@ -222,6 +231,46 @@ def quantize_experts_fp8(weights: dict) -> dict:
     return out
 
 
+def lmoe_create_mxfp4(cfg: lmoe_config, weights: lmoe_weights, experts: lmoe_mxfp4_experts, max_bt: int,
+                      stream: int = 0):
+    ctx = c_vp()
+    st = load_library().lmoe_create_mxfp4(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(experts), max_bt,
+                                          c_vp(stream), ctypes.byref(ctx))
+    return st, ctx.value
+
+
+def lmoe_quantize_mxfp4_rows(w: int, rows: int, cols: int, q: int, sf: int, stream: int = 0) -> int:
+    return load_library().lmoe_quantize_mxfp4_rows(c_vp(w), rows, cols, c_vp(q), c_vp(sf), c_vp(stream))
+
+
+def quantize_mxfp4_rows(w):
+    """MXFP4 quantization of a bf16 CUDA tensor [..., cols] by the library: returns (codes
+    uint8 [..., cols / 2], two e2m1 values per byte, and the tiled ue8m0 block scales, uint8
+    [rows * cols / 32]; rows = w.numel() / cols)."""
+    import torch
+
+    if w.dtype != torch.bfloat16 or not w.is_contiguous():
+        raise ValueError("quantize_mxfp4_rows needs a contiguous bf16 tensor")
+    cols = w.shape[-1]
+    rows = w.numel() // cols
+    # 32-byte aligned code rows (the layer's tensor maps need it); torch allocations are 512-byte aligned
+    q = torch.empty(tuple(w.shape[:-1]) + (cols // 2,), dtype=torch.uint8, device=w.device)
+    sf = torch.empty(rows * cols // 32, dtype=torch.uint8, device=w.device)
+    st = lmoe_quantize_mxfp4_rows(w.data_ptr(), rows, cols, q.data_ptr(), sf.data_ptr(),
+                                  torch.cuda.current_stream().cuda_stream)
+    if st != LMOE_OK:
+        raise LmoeError(st, "lmoe_quantize_mxfp4_rows")
+    return q, sf
+
+
+def quantize_experts_mxfp4(weights: dict) -> dict:
+    """The routed experts of a bf16 weight dict in MXFP4 (the dict lmoe_create_mxfp4 takes)."""
+    out = {}
+    for n in ("exp_gate", "exp_up", "exp_down"):
+        out[n], out[n.replace("exp_", "") + "_sf"] = quantize_mxfp4_rows(weights[n])
+    return out
+
+
 def lmoe_ffn_create(cfg: lmoe_ffn_config, w_gate: int, w_up: int, w_down: int, max_bt: int):
     ffn = c_vp()
     st = load_library().lmoe_ffn_create(ctypes.byref(cfg), c_vp(w_gate), c_vp(w_up), c_vp(w_down), max_bt,
@@ -300,19 +349,24 @@ WEIGHT_NAMES = ("w_router", "w_down", "latent_gamma", "w_up", "exp_gate", "exp_u
 class LatentMoE:
     """One layer context over borrowed torch CUDA tensors."""
 
-    def __init__(self, shape, weights: dict, max_bt: int, router_bias=None, stream=None, fp8_experts=None):
-        """fp8_experts: optional dict from quantize_experts_fp8 (e4m3 routed experts); the
-        bf16 expert weights in `weights` are then not used and may be absent."""
+    def __init__(self, shape, weights: dict, max_bt: int, router_bias=None, stream=None, fp8_experts=None,
+                 mxfp4_experts=None):
+        """fp8_experts: optional dict from quantize_experts_fp8 (e4m3 routed experts);
+        mxfp4_experts: optional dict from quantize_experts_mxfp4 (MXFP4 routed experts).  With
+        either, the bf16 expert weights in `weights` are not used and may be absent."""
         import torch
 
+        if fp8_experts is not None and mxfp4_experts is not None:
+            raise ValueError("fp8_experts and mxfp4_experts are exclusive")
+        lowp = fp8_experts if fp8_experts is not None else mxfp4_experts
         self.shape = shape
         self.dtype = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
-        self._keep = (dict(weights), dict(fp8_experts or {}))
+        self._keep = (dict(weights), dict(lowp or {}))
         self._bias = router_bias
         w = lmoe_weights()
         for n in WEIGHT_NAMES:
             t = weights.get(n)
-            if t is None and fp8_experts is not None and n.startswith("exp_"):
+            if t is None and lowp is not None and n.startswith("exp_"):
                 continue
             if not t.is_contiguous():
                 raise ValueError(f"{n} must be contiguous")
@@ -321,14 +375,21 @@ class LatentMoE:
         self.cfg = make_config(shape)
         self.max_bt = max_bt
         s = torch.cuda.current_stream() if stream is None else stream
-        if fp8_experts is None:
-            st, ctx = lmoe_create(self.cfg, w, max_bt, s.cuda_stream)
-        else:
+        if fp8_experts is not None:
             f8 = lmoe_fp8_experts(*(fp8_experts[n].data_ptr() for n in
                                     ("exp_gate", "exp_up", "exp_down", "gate_scale", "up_scale", "down_scale")))
             st, ctx = lmoe_create_fp8(self.cfg, w, f8, max_bt, s.cuda_stream)
+            what = "lmoe_create_fp8"
+        elif mxfp4_experts is not None:
+            mx = lmoe_mxfp4_experts(*(mxfp4_experts[n].data_ptr() for n in
+                                      ("exp_gate", "exp_up", "exp_down", "gate_sf", "up_sf", "down_sf")))
+            st, ctx = lmoe_create_mxfp4(self.cfg, w, mx, max_bt, s.cuda_stream)
+            what = "lmoe_create_mxfp4"
+        else:
+            st, ctx = lmoe_create(self.cfg, w, max_bt, s.cuda_stream)
+            what = "lmoe_create"
         if st != LMOE_OK:
-            raise LmoeError(st, "lmoe_create_fp8" if fp8_experts is not None else "lmoe_create")
+            raise LmoeError(st, what)
         self.ctx = ctx
 
     def _stream(self, stream):

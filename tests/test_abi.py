@@ -119,6 +119,33 @@ def test_host_side_argument_checks_of_the_widened_calls(lib):
     assert L.lmoe_quantize_fp8_rows(0x10000, -1, 16, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
     assert L.lmoe_quantize_fp8_rows(0x10000, 4, 0, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
     assert L.lmoe_quantize_fp8_rows(0x10000, 0, 16, 0x20000, 0x30000) == L.LMOE_OK
+    assert L.lmoe_quantize_mxfp4_rows(0x10000, -1, 128, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_quantize_mxfp4_rows(0x10000, 128, 0, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_quantize_mxfp4_rows(0x10000, 0, 128, 0x20000, 0x30000) == L.LMOE_OK
+    assert L.lmoe_quantize_mxfp4_rows(0x10008, 128, 128, 0x20000, 0x30000) == L.LMOE_ERR_INVALID_ARG
+    assert L.lmoe_quantize_mxfp4_rows(0x10000, 100, 128, 0x20000, 0x30000) == L.LMOE_ERR_UNSUPPORTED
+    assert L.lmoe_quantize_mxfp4_rows(0x10000, 128, 96, 0x20000, 0x30000) == L.LMOE_ERR_UNSUPPORTED
+
+
+def test_host_side_argument_checks_of_create_mxfp4(lib):
+    """lmoe_create_mxfp4: no experts, fp32 layers, misaligned codes or scales and widths that are
+    not multiples of 128 are rejected on the host, before any CUDA call."""
+    def mx(**kw):
+        e = L.lmoe_mxfp4_experts(*([0x20000] * 6))
+        for k, v in kw.items():
+            setattr(e, k, v)
+        return e
+    out = ctypes.c_void_p()
+    assert lib.lmoe_create_mxfp4(ctypes.byref(_cfg()), ctypes.byref(_weights()), None, 64, None,
+                                 ctypes.byref(out)) == L.LMOE_ERR_INVALID_ARG and not out.value
+    for cfg, e, status in [(_cfg(dtype=L.LMOE_F32), mx(), L.LMOE_ERR_INVALID_ARG),
+                           (_cfg(), mx(exp_up=0x20010), L.LMOE_ERR_INVALID_ARG),
+                           (_cfg(), mx(down_sf=0x20008), L.LMOE_ERR_INVALID_ARG),
+                           (_cfg(), mx(gate_sf=None), L.LMOE_ERR_INVALID_ARG),
+                           (_cfg(latent=192), mx(), L.LMOE_ERR_UNSUPPORTED),
+                           (_cfg(expert_inter=448), mx(), L.LMOE_ERR_UNSUPPORTED)]:
+        st, ctx = L.lmoe_create_mxfp4(cfg, _weights(), e, 64)
+        assert st == status and not ctx, (st, status)
 
 
 def _create_null_cfg(env):

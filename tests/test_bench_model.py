@@ -62,6 +62,18 @@ def test_fp8_experts_byte_model():
     assert g == 896 * 2 * 3072 * (3584 + 4)
 
 
+def test_mxfp4_experts_byte_model():
+    """MXFP4 experts: half a byte per expert weight plus one scale byte per 32 weights (17/32 byte
+    per weight, 29.6 G weights -> 15.7 GB); the rest of the layer stays bf16; FLOPs are unchanged."""
+    f16, b16, _ = bench.algorithmic(FULL, 8192, 896)
+    f4, b4, st4 = bench.algorithmic(FULL, 8192, 896, mxfp4_experts=True)
+    assert f4 == f16
+    expert_params = 896 * 3 * 3584 * 3072
+    assert b16 - b4 == pytest.approx(expert_params * (2 - 17 / 32), rel=1e-12)
+    assert st4["expert_gate_up_gemm"][1] == pytest.approx(896 * 2 * 3072 * 3584 * 17 / 32, rel=1e-12)
+    assert st4["expert_gate_up_gemm"][1] + st4["expert_down_gemm"][1] == pytest.approx(15.73e9, rel=1e-3)
+
+
 def test_layer_fraction_takes_the_binding_roof():
     """The layer line's `bound` is the roof with the larger ideal time and `frac` its fraction:
     at 8192 tokens the 59.8 GB of weights and rows bind (HBM), at 16384 the 23.5 TFLOP do."""
