@@ -21,7 +21,7 @@
 // 128 tokens takes one slot (A0 in its first 128 columns, A1 in the second), so two such
 // tiles double-buffer; a wider tile takes both slots (A0 in slot 0, A1 in slot 1).
 // Roles (512 threads): warp 0 streams weight tiles through a 4-stage ring, warp 2 streams
-// token tiles through a kTStages ring (TMA, mbarrier completion), warp 1 owns TMEM and
+// token tiles through a 3-stage ring (TMA, mbarrier completion), warp 1 owns TMEM and
 // issues tcgen05.mma (one thread), warps 4-15 drain the accumulators with tcgen05.ld (three
 // warps per TMEM lane quadrant, taking every third 32-token chunk) and write the outputs.
 // While a wide tile drains, the next one cannot start, so the epilogue packs its results
@@ -48,7 +48,7 @@ constexpr int kTokMax = kTileM;                  // tokens per tile of the group
 constexpr int kTokBox = 16;                      // token rows per TMA box
 constexpr int kHalfBytes = kHalf * kBK * 2;      // 16 KB
 constexpr int kWStageBytes = 2 * kHalfBytes;     // 32 KB of weights per stage
-constexpr int kTStages = 3;
+constexpr int kTStagesDefault = 3;
 constexpr int kSlotCols = 256;
 constexpr int kEpiWarps = 12;
 constexpr int kEpiThreads = 32 * kEpiWarps;
@@ -67,6 +67,19 @@ constexpr int kMxSfBytes = 512;                  // MXFP4: block scales of 128 r
 constexpr int kMxNarrow = 64;
 constexpr uint32_t kMxSfaCol = 192;
 constexpr uint32_t kMxSfbCol = 448;
+// MXFP4 at small batches (no expert with more than kSwapTok tokens): the operands swap roles.  At a
+// few tokens an MMA takes the time its A operand needs to leave shared memory (128 rows x 32 bytes
+// per K step), and a padded MXFP4 weight tile carries only 2 KB of codes in those 4 KB, so with the
+// weights as A the codes would stream at half the bf16 rate.  Here the tokens are A (M = 128 rows;
+// rows past the tile's tokens hold stale bytes whose results are never read) and the 256 weight
+// rows of a stage are B (N = 256, fetched twice as fast per row).  The accumulator is one
+// 256-column slot (lane = token, column = weight row); the tokens' unit scales and the weight
+// stages' scales take the columns after it.
+constexpr int kSwapTok = 128;
+constexpr int kSwapWStages = 5;
+constexpr uint32_t kSwapSfaCol = 256;
+constexpr uint32_t kSwapSfbCol = 264;
+
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
 
@@ -74,10 +87,15 @@ constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a tim
 // token tiles of up to 256 (more MMA work per k-block to cover the L2 round trip of their
 // operands) and need no expert schedule; grouped ones keep tiles of kTokMax tokens and the
 // schedule.
-template <bool DENSE, bool MX = false>
+// MXV: 0 = bf16 / e4m3 weights, 1 = MXFP4 weights, 2 = MXFP4 weights at small batches with the
+// operands swapped (token tiles of at most kSwapTok tokens, held as 128-row MMA operands).
+template <bool DENSE, int MXV = 0>
 struct Geo {
-  static constexpr int kTok = DENSE ? 256 : kTokMax;             // tokens per tile at most
-  static constexpr int kWStages = 4;                             // weight ring (32 KB stages)
+  static constexpr bool kMx = MXV != 0, kSwap = MXV == 2;
+  static constexpr int kTok = DENSE ? 256 : kSwap ? kSwapTok : kTokMax;   // tokens per tile at most
+  static constexpr int kWStages = kSwap ? kSwapWStages : 4;      // weight ring (32 KB stages)
+  static constexpr int kTStages = kTStagesDefault;               // token ring
+  static constexpr bool kSchedSmem = !DENSE;                     // expert schedule in shared memory
   // barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
   static constexpr int kNumBars = 2 * kWStages + 2 * kTStages + 4 + 1;
   static constexpr int kTStageBytes = kTok * kBK * 2;            // token rows per stage
@@ -85,9 +103,9 @@ struct Geo {
   static constexpr int kOffT = kWStages * kWStageBytes;
   // MXFP4: the weight stages' block scales (512 bytes per operand) and the tokens' unit scales
   static constexpr int kOffSf = kOffT + kTStages * kTStageBytes;
-  static constexpr int kOffSfUnit = kOffSf + (MX ? kWStages * 2 * kMxSfBytes : 0);
-  static constexpr int kOffSched = kOffSfUnit + (MX ? kMxSfBytes : 0);
-  static constexpr int kOffBars = kOffSched + (DENSE ? 0 : 2 * kSchedMax * 4);
+  static constexpr int kOffSfUnit = kOffSf + (kMx ? kWStages * 2 * kMxSfBytes : 0);
+  static constexpr int kOffSched = kOffSfUnit + (kMx ? kMxSfBytes : 0);
+  static constexpr int kOffBars = kOffSched + (kSchedSmem ? 2 * kSchedMax * 4 : 0);
   static constexpr int kOffMisc = kOffBars + kNumBars * 8;
   static constexpr int kSmemBytes = 1024 + kOffMisc + 16;
   static_assert(kTok % 16 == 0 && kTok <= 256, "MMA N limit");
@@ -305,6 +323,10 @@ __device__ __forceinline__ uint32_t idesc_mx(int m, int n) {
   return (5u << 7) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24);
 }
 __device__ __forceinline__ uint32_t mx_sf_id(uint32_t j) { return (j << 4) | (j << 29); }
+// The same with the operands swapped: A format 0 = e4m3 tokens, B format 5 = e2m1 weights.
+__device__ __forceinline__ uint32_t idesc_mx_swap(int m, int n) {
+  return (5u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) | ((uint32_t)(m >> 4) << 24);
+}
 
 // tanh by the MUFU hardware approximation (PTX tanh.approx.f32).
 __device__ __forceinline__ float tanh_hw(float x) {
@@ -434,13 +456,14 @@ __device__ __forceinline__ uint32_t acc_col(bool wide, int slot, int h) {
 }
 
 // ------------------------------------------------------------------ the kernel
-template <int EPI, bool F8, bool DENSE, bool SPLIT, bool MX>
+template <int EPI, bool F8, bool DENSE, bool SPLIT, int MXV>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  constexpr bool MX = MXV != 0, SWAP = MXV == 2;
   static_assert(!SPLIT || (DENSE && !F8), "split-K covers the dense bf16 GEMMs");
   static_assert(!MX || (F8 && !DENSE && !SPLIT && EPI != kEpiRouter), "MXFP4 covers the routed-expert GEMMs");
   static_assert(kTokMax <= (int)kMxSfaCol, "MXFP4 scale columns lie past the widest accumulator");
-  using G = Geo<DENSE, MX>;
+  using G = Geo<DENSE, MXV>;
   constexpr int kBKe = F8 ? 2 * kBK : kBK;   // K elements per stage (128-byte rows)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -459,21 +482,21 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   auto wfull_bar = [&](int s) { return bar0 + 8u * s; };
   auto wempty_bar = [&](int s) { return bar0 + 8u * (G::kWStages + s); };
   auto tfull_bar = [&](int s) { return bar0 + 8u * (2 * G::kWStages + s); };
-  auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * G::kWStages + kTStages + s); };
-  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * G::kWStages + 2 * kTStages + a); };
-  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * G::kWStages + 2 * kTStages + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * G::kWStages + 2 * kTStages + 4);
+  auto tempty_bar = [&](int s) { return bar0 + 8u * (2 * G::kWStages + G::kTStages + s); };
+  auto afull_bar = [&](int a) { return bar0 + 8u * (2 * G::kWStages + 2 * G::kTStages + a); };
+  auto aempty_bar = [&](int a) { return bar0 + 8u * (2 * G::kWStages + 2 * G::kTStages + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * G::kWStages + 2 * G::kTStages + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::kWStages; ++s) { mbar_init(wfull_bar(s), 1); mbar_init(wempty_bar(s), 1); }
-    for (int s = 0; s < kTStages; ++s) { mbar_init(tfull_bar(s), 1); mbar_init(tempty_bar(s), 1); }
+    for (int s = 0; s < G::kTStages; ++s) { mbar_init(tfull_bar(s), 1); mbar_init(tempty_bar(s), 1); }
     for (int a = 0; a < 2; ++a) { mbar_init(afull_bar(a), 1); mbar_init(aempty_bar(a), kEpiWarps); }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  const bool sched_smem = !DENSE && p.G > 0 && p.G < kSchedMax;
+  const bool sched_smem = G::kSchedSmem && p.G > 0 && p.G < kSchedMax;
   if (sched_smem) {
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
       s_seg[i] = p.seg_off[i];
@@ -571,6 +594,15 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const int ntr = (tl.ntok + 15) & ~15;
       const int nbox = ntr / kTokBox;
       const int rot = SPLIT ? 0 : k_start(p, tl);
+      if (SWAP && tl.ntok > G::kTok) {
+        // the host launches this variant only when no expert has more tokens than its stages hold
+        if (lane == 0) {
+          atomicOr(p.status, kStatusAssert);
+          *abort_flag = 1;
+        }
+        stop = true;
+        break;
+      }
       for (int kb = kb0; kb < kb1; ++kb) {
         bool ok = true;
         if (lane == 0) ok = mbar_wait(tempty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns);
@@ -579,7 +611,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         pending &= ~(1u << stage);
         if (p.inject) {
           // test hook: nothing fills this stage, so its consumer's bounded wait runs out
-          if (++stage == kTStages) { stage = 0; phase ^= 1u; }
+          if (++stage == G::kTStages) { stage = 0; phase ^= 1u; }
           continue;
         }
         if (lane == 0) mbar_expect_tx(tfull_bar(stage), (uint32_t)ntr * (kBK * 2));
@@ -591,11 +623,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
                       tfull_bar(stage), tpol);
         pending |= 1u << stage;
         pend_parity = (pend_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kTStages) { stage = 0; phase ^= 1u; }
+        if (++stage == G::kTStages) { stage = 0; phase ^= 1u; }
       }
     }
     if (stop && lane == 0) {
-      for (int s = 0; s < kTStages; ++s)
+      for (int s = 0; s < G::kTStages; ++s)
         if (pending & (1u << s)) mbar_wait(tfull_bar(s), (pend_parity >> s) & 1u, abort_flag, p.status, p.timeout_ns, false);
     }
     __syncwarp();
@@ -606,7 +638,11 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       uint32_t wph = 0, tph = 0;
       uint32_t aph[2] = {0u, 0u};
       bool stop = false, issued = false;
-      if (MX) {
+      if (SWAP) {
+        // unit scales of the token operand (A, 128 rows): 4 columns
+        tc_cp_sf(tmem_base + kSwapSfaCol, sf_desc(sfunit));
+        issued = true;
+      } else if (MX) {
         // unit scales of the token operand, 8 columns (up to 256 tokens)
         tc_cp_sf(tmem_base + kMxSfbCol, sf_desc(sfunit));
         tc_cp_sf(tmem_base + kMxSfbCol + 4u, sf_desc(sfunit));
@@ -618,6 +654,36 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
         const int ntr = (tl.ntok + 15) & ~15;
         const bool wide = ntr > (MX ? kMxNarrow : kHalf);
         const int nh = tile_halves<EPI>(p, tl);
+        if (SWAP) {
+          // D[token, weight row] in one 256-column slot: A = the 128-row token stage, B = the
+          // stage's nh * 128 weight rows, B's scales moved to this stage's TMEM columns first
+          if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
+          tc_fence_after();
+          const uint32_t idesc_s = idesc_mx_swap(kHalf, nh * kHalf);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(wfull_bar(ws), wph, abort_flag, p.status, p.timeout_ns) ||
+                !mbar_wait(tfull_bar(ts), tph, abort_flag, p.status, p.timeout_ns)) { stop = true; break; }
+            tc_fence_after();
+            const uint64_t td = smem_desc(tbase + ts * G::kTStageBytes);
+            const uint64_t wd = smem_desc(wbase + ws * kWStageBytes);
+            const uint32_t sfb = tmem_base + kSwapSfbCol + 8u * ws;
+            tc_cp_sf(sfb, sf_desc(sfbase + (uint32_t)(ws * 2) * kMxSfBytes));
+            if (nh == 2) tc_cp_sf(sfb + 4u, sf_desc(sfbase + (uint32_t)(ws * 2 + 1) * kMxSfBytes));
+#pragma unroll
+            for (int j = 0; j < kBK / 16; ++j)
+              tc_mma_mx(tmem_base, td + 2u * j, wd + 2u * j, idesc_s | mx_sf_id(j), (kb != kb0 || j != 0) ? 1u : 0u,
+                        tmem_base + kSwapSfaCol, sfb);
+            issued = true;
+            tc_commit(wempty_bar(ws));
+            tc_commit(tempty_bar(ts));
+            if (++ws == G::kWStages) { ws = 0; wph ^= 1u; }
+            if (++ts == G::kTStages) { ts = 0; tph ^= 1u; }
+          }
+          if (stop) break;
+          tc_commit(afull_bar(0));
+          aph[0] ^= 1u;
+          continue;
+        }
         const uint32_t idesc = MX ? idesc_mx(kHalf, ntr) : F8 ? idesc_e4m3(kHalf, ntr) : idesc_bf16(kHalf, ntr);
         if (wide) {
           if (!mbar_wait(aempty_bar(0), aph[0] ^ 1u, abort_flag, p.status, p.timeout_ns) ||
@@ -666,7 +732,7 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
           tc_commit(wempty_bar(ws));
           tc_commit(tempty_bar(ts));
           if (++ws == G::kWStages) { ws = 0; wph ^= 1u; }
-          if (++ts == kTStages) { ts = 0; tph ^= 1u; }
+          if (++ts == G::kTStages) { ts = 0; tph ^= 1u; }
         }
         if (stop) break;
         if (wide) {
@@ -699,6 +765,80 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const int ntr = (tl.ntok + 15) & ~15;
       const bool wide = ntr > (MX ? kMxNarrow : kHalf);
       const int nh = tile_halves<EPI>(p, tl);
+      if (SWAP) {
+        // lane = token q * 32 + lane of the tile; this warp takes the 32-column chunks sub, sub + 3, ...
+        // GLU: gate columns [0, 128), up columns [128, 256) -> 32 e4m3 activations per chunk;
+        // store: nh * 128 output columns -> 32 bf16 values per chunk.  TMEM is released before the
+        // stores; each lane then writes its token's row segments (32 or 64 contiguous bytes).
+        const bool ok = mbar_wait(afull_bar(0), aph[0], abort_flag, p.status, p.timeout_ns);
+        if (named_sync_or(1, kEpiThreads, !ok || *abort_flag)) break;
+        tc_fence_after();
+        const int tok = q * 32 + lane;
+        const bool live = tok < tl.ntok;
+        uint32_t res[3][16];
+        const int nchunk = EPI == kEpiGlu ? 4 : nh * 4;
+        if (EPI == kEpiGlu) {
+          const float ts = live ? p.tscale[p.perm[tl.tok0 + tok]] : 0.f;
+#pragma unroll
+          for (int nc = 0; nc < 2; ++nc) {
+            const int c = sub + 3 * nc;
+            if (c >= nchunk) break;
+            uint32_t g[32], u[32];
+            tmem_ld32(lane_base + c * 32, g);
+            tmem_ld32(lane_base + kHalf + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+              uint32_t word = 0;
+#pragma unroll
+              for (int b = 0; b < 4; ++b) {
+                const float a = situ_glu_fast(__uint_as_float(g[j + b]) * ts, __uint_as_float(u[j + b]) * ts, p);
+                word |= (uint32_t)e4m3_byte(a * p.h_mul) << (8 * b);
+              }
+              res[nc][j >> 2] = word;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int nc = 0; nc < 3; ++nc) {
+            const int c = sub + 3 * nc;
+            if (c >= nchunk) break;
+            uint32_t v[32];
+            tmem_ld32(lane_base + c * 32, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              res[nc][j] = pack_bf16x2(__uint_as_float(v[2 * j]) * p.out_mul, __uint_as_float(v[2 * j + 1]) * p.out_mul);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(aempty_bar(0));
+        aph[0] ^= 1u;
+        if (live) {
+          const long long row = tl.tok0 + tok;
+          if (EPI == kEpiGlu) {
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+              const int c = sub + 3 * k;
+              if (c >= nchunk) break;
+              uint4* o = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) + row * p.ldo + tl.fb * kHalf + c * 32);
+              o[0] = make_uint4(res[k][0], res[k][1], res[k][2], res[k][3]);
+              o[1] = make_uint4(res[k][4], res[k][5], res[k][6], res[k][7]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+              const int c = sub + 3 * k;
+              if (c >= nchunk) break;
+              uint4* o = reinterpret_cast<uint4*>(static_cast<bf16*>(p.out) + row * p.ldo + tl.fb * 2 * kHalf + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) o[v] = make_uint4(res[k][4 * v], res[k][4 * v + 1], res[k][4 * v + 2], res[k][4 * v + 3]);
+            }
+          }
+        }
+        continue;
+      }
       bool ok;
       if (wide) ok = mbar_wait(afull_bar(0), aph[0], abort_flag, p.status, p.timeout_ns) &&
                      mbar_wait(afull_bar(1), aph[1], abort_flag, p.status, p.timeout_ns);
@@ -1012,9 +1152,9 @@ int dense_tok_tile(int bt, int n_fb, int grid) {
   return best;
 }
 
-template <int EPI, bool F8, bool DENSE, bool SPLIT = false, bool MX = false>
+template <int EPI, bool F8, bool DENSE, bool SPLIT = false, int MXV = 0>
 cudaError_t launch_kernel(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t st) {
-  tc_gemm_kernel<EPI, F8, DENSE, SPLIT, MX><<<grid, kThreads, Geo<DENSE, MX>::kSmemBytes, st>>>(maps, p);
+  tc_gemm_kernel<EPI, F8, DENSE, SPLIT, MXV><<<grid, kThreads, Geo<DENSE, MXV>::kSmemBytes, st>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -1036,7 +1176,7 @@ cudaError_t launch_split(const TcMaps& maps, const TcParams& p, int grid, int sm
 // (p.part) is split along K into up to SMs / tiles work items per tile (each of at least
 // kSplitMinKb k-blocks) and reduced by a second kernel.  *n = kernels launched.
 cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cudaStream_t st, bool f8, int* n,
-                      bool mx = false) {
+                      int mxv = 0) {
   *n = 0;
   p.ksplit = 1;
   if (p.G == 0) p.tok_tile = dense_tok_tile(p.bt, p.n_fb, sm_count);
@@ -1052,9 +1192,13 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
   }
   if (grid <= 0) return cudaSuccess;
   *n = p.ksplit > 1 ? 2 : 1;
-  if (mx) {   // the MXFP4 routed experts (grouped)
-    if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false, false, true>(maps, p, grid, st);
-    return launch_kernel<kEpiStore, true, false, false, true>(maps, p, grid, st);
+  if (mxv == 2) {   // the MXFP4 routed experts at small batches, operands swapped (at most kSwapTok tokens per expert)
+    if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false, false, 2>(maps, p, grid, st);
+    return launch_kernel<kEpiStore, true, false, false, 2>(maps, p, grid, st);
+  }
+  if (mxv == 1) {   // the MXFP4 routed experts (grouped)
+    if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false, false, 1>(maps, p, grid, st);
+    return launch_kernel<kEpiStore, true, false, false, 1>(maps, p, grid, st);
   }
   if (f8) {   // the fp8 routed experts (grouped)
     if (epi == kEpiGlu) return launch_kernel<kEpiGlu, true, false>(maps, p, grid, st);
@@ -1078,10 +1222,10 @@ cudaError_t launch_tc(const TcMaps& maps, TcParams& p, int epi, int sm_count, cu
   }
 }
 
-template <int EPI, bool F8, bool DENSE, bool SPLIT = false, bool MX = false>
+template <int EPI, bool F8, bool DENSE, bool SPLIT = false, int MXV = 0>
 cudaError_t set_smem() {
-  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE, SPLIT, MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Geo<DENSE, MX>::kSmemBytes);
+  return cudaFuncSetAttribute(tc_gemm_kernel<EPI, F8, DENSE, SPLIT, MXV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Geo<DENSE, MXV>::kSmemBytes);
 }
 
 // Raises the dynamic shared-memory limit of every kernel instance a plan launches.
@@ -1096,8 +1240,10 @@ cudaError_t prepare_kernels(bool f8, bool mx = false) {
   if (e == cudaSuccess) e = set_smem<kEpiGlu, false, false>();
   if (e == cudaSuccess && f8) e = set_smem<kEpiGlu, true, false>();
   if (e == cudaSuccess && f8) e = set_smem<kEpiStore, true, false>();
-  if (e == cudaSuccess && mx) e = set_smem<kEpiGlu, true, false, false, true>();
-  if (e == cudaSuccess && mx) e = set_smem<kEpiStore, true, false, false, true>();
+  if (e == cudaSuccess && mx) e = set_smem<kEpiGlu, true, false, false, 1>();
+  if (e == cudaSuccess && mx) e = set_smem<kEpiStore, true, false, false, 1>();
+  if (e == cudaSuccess && mx) e = set_smem<kEpiGlu, true, false, false, 2>();
+  if (e == cudaSuccess && mx) e = set_smem<kEpiStore, true, false, false, 2>();
   return e;
 }
 
@@ -1308,7 +1454,8 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* 
   }
   if (!ok) return cudaErrorInvalidValue;
   p.n_fb = epi == kEpiGlu ? (a.N + kHalf - 1) / kHalf : (a.N + 2 * kHalf - 1) / (2 * kHalf);
-  return launch_tc(maps, p, epi, pl->sm_count, st, f8, n, f8 && pl->mx);
+  // a call of at most kSwapTok tokens gives no expert more (top-K experts are distinct per token)
+  return launch_tc(maps, p, epi, pl->sm_count, st, f8, n, !(f8 && pl->mx) ? 0 : a.bt_tokens <= kSwapTok ? 2 : 1);
 }
 
 // ------------------------------------------------------------------ dense SiTU-GLU FFN

@@ -601,6 +601,7 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     g.seg_k0[1] = c.expert_inter; g.seg_B[0] = ctx->w.exp_down; g.seg_ldb[0] = c.expert_inter;
     g.b_group_rows = c.latent;
     g.seg_off = ctx->offsets; g.mtile_off = ctx->mtile_off; g.G = c.n_experts; g.max_mtiles = max_mtiles;
+    g.bt_tokens = bt;
     g.epi = kEpiStore; g.out = ctx->y; g.ldo = c.latent;
     g.op = kOpExpertDown;
     e = run_gemm(ctx, g, st);
