@@ -6,14 +6,14 @@
 // scaling: the weights' ue8m0 block scales go to TMEM by tcgen05.cp before each stage's MMAs).
 //
 // Weight-stationary tiles.  A tile is 256 weight rows (two MMA operands A0, A1 of M = 128
-// rows each) against up to kTokMax tokens (the MMA's N side, shared by both MMAs), with K
+// rows each) against up to 256 tokens (192 for MXFP4; the MMA's N side, shared by both MMAs), with K
 // stepped one 128-byte swizzle row at a time (64 bf16 or 128 e4m3 values):
 //   * GLU tiles: A0 = 128 gate rows, A1 = the 128 up rows of the same output features, so
 //     one TMEM lane holds both branches of a feature and the SiTU-GLU epilogue needs no
 //     exchange between warps;
 //   * store tiles: A0, A1 = two consecutive blocks of 128 output rows (A1 is skipped when
 //     it lies past the last output row);
-//   * an expert segment is covered by token tiles of kTokMax and one last tile rounded up
+//   * an expert segment is covered by full token tiles and one last tile rounded up
 //     to a multiple of 16 tokens, so each weight tile is streamed from HBM once per token
 //     tile (once per expert at prefill sizes), and each token row is re-read from L2 once
 //     per 128 output features.
@@ -27,7 +27,8 @@
 // While a wide tile drains, the next one cannot start, so the epilogue packs its results
 // into registers and releases TMEM before the global stores, and SiTU-GLU uses the
 // hardware tanh approximation (relative error about 2^-11, below the bf16 rounding of its
-// output).  The expert tile schedule is copied into shared memory once per CTA.  Every
+// output).  The MXFP4 kernels copy the expert tile schedule into shared memory once per CTA;
+// the others read it through L1 (their 256-token stages leave no room).  Every
 // mbarrier wait is bounded: on expiry the kernel records the timeout status, drains what it
 // issued and returns.
 #include <cuda.h>
@@ -44,7 +45,8 @@ namespace {
 
 constexpr int kBK = 64;
 constexpr int kHalf = 128;                       // weight rows per MMA (M)
-constexpr int kTokMax = kTileM;                  // tokens per tile of the grouped GEMMs (MMA N)
+constexpr int kTokMax = kTileM;                  // tokens per tile of the grouped MXFP4 GEMMs (MMA N)
+constexpr int kTokGroup = kTileWide;             // tokens per tile of the grouped bf16 / e4m3 GEMMs
 constexpr int kTokBox = 16;                      // token rows per TMA box
 constexpr int kHalfBytes = kHalf * kBK * 2;      // 16 KB
 constexpr int kWStageBytes = 2 * kHalfBytes;     // 32 KB of weights per stage
@@ -83,19 +85,21 @@ constexpr uint32_t kSwapSfbCol = 264;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;   // 2 s per wait
 constexpr unsigned long long kInjectTimeoutNs = 20000000ull; // 20 ms when a timeout is injected
 
-// Shared-memory layout of the grouped (routed experts) and dense launches.  Dense GEMMs take
-// token tiles of up to 256 (more MMA work per k-block to cover the L2 round trip of their
-// operands) and need no expert schedule; grouped ones keep tiles of kTokMax tokens and the
-// schedule.
+// Shared-memory layout of the grouped (routed experts) and dense launches.  Dense GEMMs and the
+// grouped bf16 / e4m3 GEMMs take token tiles of up to 256 (a weight tile's MMAs take about the
+// same time for any token count up to 256, so fewer, wider tiles mean less MMA time per token);
+// the grouped ones then read their expert schedule through L1.  The grouped MXFP4 GEMMs keep tiles
+// of kTokMax tokens (TMEM columns past them hold the block scales) and the schedule in shared
+// memory.
 // MXV: 0 = bf16 / e4m3 weights, 1 = MXFP4 weights, 2 = MXFP4 weights at small batches with the
 // operands swapped (token tiles of at most kSwapTok tokens, held as 128-row MMA operands).
 template <bool DENSE, int MXV = 0>
 struct Geo {
   static constexpr bool kMx = MXV != 0, kSwap = MXV == 2;
-  static constexpr int kTok = DENSE ? 256 : kSwap ? kSwapTok : kTokMax;   // tokens per tile at most
+  static constexpr int kTok = DENSE ? 256 : kSwap ? kSwapTok : kMx ? kTokMax : kTokGroup;   // tokens per tile at most
   static constexpr int kWStages = kSwap ? kSwapWStages : 4;      // weight ring (32 KB stages)
   static constexpr int kTStages = kTStagesDefault;               // token ring
-  static constexpr bool kSchedSmem = !DENSE;                     // expert schedule in shared memory
+  static constexpr bool kSchedSmem = !DENSE && kMx;              // expert schedule in shared memory
   // barriers: W full/empty, T full/empty, TMEM full/empty per slot, drain
   static constexpr int kNumBars = 2 * kWStages + 2 * kTStages + 4 + 1;
   static constexpr int kTStageBytes = kTok * kBK * 2;            // token rows per stage
@@ -128,11 +132,11 @@ struct TcParams {
   int n_fb;                 // feature blocks (256 output rows, or 128 GLU outputs)
   int kblocks;              // K / 64
   int bt;                   // dense: tokens
-  int tok_tile;             // dense: tokens per tile (<= kTokMax, multiple of 16)
+  int tok_tile;             // tokens per tile: dense (multiple of 16, <= 256), grouped (the schedule's tile size)
   int ksplit;               // dense: work items per tile, each over its own K range (1 = whole K)
   float* part;              // split-K: fp32 accumulators, kPartItem per work item
   const int32_t* seg_off;   // grouped: [G + 1] token segments
-  const int32_t* mtile_off; // grouped: [G + 1] prefix of kTokMax-token tiles
+  const int32_t* mtile_off; // grouped: [G + 1] prefix of tok_tile-token tiles
   int G;                    // grouped: number of groups, 0 for dense
   void* out;
   long long ldo;
@@ -395,8 +399,8 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int32_t* se
     r.g = lo;
     r.fb = local / nt;
     const int tb = local - r.fb * nt;
-    r.tok0 = seg[lo] + tb * kTokMax;
-    r.ntok = min(kTokMax, seg[lo + 1] - r.tok0);
+    r.tok0 = seg[lo] + tb * p.tok_tile;
+    r.ntok = min(p.tok_tile, seg[lo + 1] - r.tok0);
   } else {
     const int nt = (p.bt + p.tok_tile - 1) / p.tok_tile;
     const int grp = t / (kDenseGroup * p.n_fb);
@@ -594,8 +598,9 @@ tc_gemm_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
       const int ntr = (tl.ntok + 15) & ~15;
       const int nbox = ntr / kTokBox;
       const int rot = SPLIT ? 0 : k_start(p, tl);
-      if (SWAP && tl.ntok > G::kTok) {
-        // the host launches this variant only when no expert has more tokens than its stages hold
+      if (tl.ntok > G::kTok) {
+        // the schedule's tiles never exceed the stages (the host matches them; the swapped MXFP4
+        // kernels run only for calls of at most kSwapTok tokens)
         if (lane == 0) {
           atomicOr(p.status, kStatusAssert);
           *abort_flag = 1;
@@ -1327,6 +1332,8 @@ void tc_plan_destroy(TcPlan* plan) { delete plan; }
 
 void tc_inject_wait_timeout(TcPlan* plan) { plan->inject = true; }
 
+int tc_group_tile(const TcPlan* plan) { return plan->mx ? kTileM : kTileWide; }
+
 cudaError_t tc_gather_tokens(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* n) {
   const lmoe_config& c = pl->cfg;
   const void* rows = pl->buf.z;
@@ -1429,6 +1436,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* 
       p.seg_off = a.seg_off;
       p.mtile_off = a.mtile_off;
       p.G = a.G;
+      p.tok_tile = tc_group_tile(pl);
       break;
     }
     case kOpExpertDown:
@@ -1448,6 +1456,7 @@ cudaError_t launch_gemm_tc(TcPlan* pl, const GemmArgs& a, cudaStream_t st, int* 
       p.seg_off = a.seg_off;
       p.mtile_off = a.mtile_off;
       p.G = a.G;
+      p.tok_tile = tc_group_tile(pl);
       break;
     default:
       return cudaErrorInvalidValue;

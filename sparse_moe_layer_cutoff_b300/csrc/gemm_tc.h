@@ -33,6 +33,9 @@ void tc_plan_destroy(TcPlan* plan);
 // shortens its waits to 20 ms, so the kernel times out, records LMOE timeout status and
 // returns.
 void tc_inject_wait_timeout(TcPlan* plan);
+// Tokens per tile of the routed-expert GEMMs: the granularity of the m-tile prefix the routing
+// tail must write for this plan (kTileWide for bf16 / e4m3 experts, kTileM for MXFP4).
+int tc_group_tile(const TcPlan* plan);
 // One GemmOp; *n = kernels launched (a dense GEMM split along K adds its reduction).
 cudaError_t launch_gemm_tc(TcPlan* plan, const GemmArgs& a, cudaStream_t st, int* n);
 // fp32 values of TcBuffers::part per SM

@@ -10,7 +10,9 @@ constexpr int kMaxExperts = 4096;
 constexpr int kMaxTopK = 64;
 constexpr int kMaxShared = 3;
 constexpr int kSegTokens = 128;   // tokens per block of the segmentation kernels
-constexpr int kTileM = 192;       // tokens per grouped GEMM tile (m-tile prefix granularity)
+constexpr int kTileM = 192;       // tokens per grouped GEMM tile (m-tile prefix granularity): CUDA-core
+                                  // engine and MXFP4 experts
+constexpr int kTileWide = 256;    // tokens per grouped tensor-core tile of the bf16 and e4m3 experts
 
 struct RouteArgs {
   const float* logits;      // [bt, E]

@@ -269,7 +269,7 @@ cudaError_t route_impl(lmoe_ctx* ctx, const void* x, int bt, cudaStream_t st, in
   stage_mark(ctx, 1, st);
   RouteArgs r;
   r.logits = ctx->logits; r.logits_t = ctx->logits_t;
-  r.bt = bt; r.n_experts = c.n_experts; r.top_k = c.top_k; r.tile_m = kTileM;
+  r.bt = bt; r.n_experts = c.n_experts; r.top_k = c.top_k; r.tile_m = ctx->use_tc ? tc_group_tile(ctx->tc) : kTileM;
   r.alpha = ctx->alpha; r.idx = ctx->idx; r.w = ctx->wk;
   r.block_cnt = ctx->block_cnt; r.counts = ctx->counts; r.offsets = ctx->offsets;
   r.mtile_off = ctx->mtile_off; r.perm = ctx->perm; r.inv = ctx->inv;
@@ -563,7 +563,8 @@ static lmoe_status forward_entry(lmoe_ctx* ctx, const void* x, int32_t bt, void*
     }
   }
   const long long ldc = (long long)c.latent + (long long)c.n_shared * c.shared_inter;
-  const int max_mtiles = (int)(((long long)bt * c.top_k) / kTileM + c.n_experts + 1);  // >= sum of ceil(cnt/kTileM)
+  const int tile_m = ctx->use_tc ? tc_group_tile(ctx->tc) : kTileM;
+  const int max_mtiles = (int)(((long long)bt * c.top_k) / tile_m + c.n_experts + 1);  // >= sum of ceil(cnt/tile_m)
 
   if (e == cudaSuccess) {  // z = x W_down^T
     GemmArgs g = base_args(ctx);
