@@ -103,8 +103,9 @@ def _run_fp8(wl, bt, rows=None, norm="expert"):
     layer.close()
 
 
-@pytest.mark.parametrize("bt", [300, 1, 77])
+@pytest.mark.parametrize("bt", [300, 1, 77, 2048])
 def test_fp8_layer_small_matches_oracle(bt):
+    """2048 tokens give experts of ~256 tokens: full 256-token tiles and experts of several tiles."""
     _run_fp8(WORKLOADS["small_bf16"], bt)
 
 

@@ -121,10 +121,11 @@ def _run_mx(wl, bt, rows=None):
     return m, rl
 
 
-@pytest.mark.parametrize("bt", [300, 1, 77, 128, 129])
+@pytest.mark.parametrize("bt", [300, 1, 77, 128, 129, 2048])
 def test_mxfp4_layer_small_matches_oracle(bt):
     """Calls of 128 tokens or fewer run the expert GEMMs with the operands swapped (tokens as the
-    MMA's A side), larger ones with the weights as A."""
+    MMA's A side), larger ones with the weights as A (at 2048 tokens experts span several
+    192-token tiles)."""
     _run_mx(WORKLOADS["small_bf16"], bt)
 
 
