@@ -208,7 +208,7 @@ LMOE_API lmoe_status lmoe_set_cutoff_momentum(lmoe_ctx* ctx, double momentum);
  * LMOE_NORM_COMBINED normalises the weighted sum once, in front of W_up ("Vue d'ensemble de
  * l'architecture", "Par où l'information passe, pour un seul jeton", step f "RMSNorm + W_up"):
  *     c = gamma * s / rms(s),  s = sum_k w_k * y_k,  rms(v) = sqrt(mean(v^2) + rms_eps).
- * Applies to every later lmoe_forward on this context (bf16, fp32 and fp8-expert layers).
+ * Applies to every later lmoe_forward on this context (bf16, fp32, fp8- and MXFP4-expert layers).
  * Returns LMOE_ERR_INVALID_ARG for a NULL context or an unknown placement,
  * LMOE_ERR_UNSUPPORTED for LMOE_NORM_COMBINED with latent > 49152, LMOE_ERR_CUDA if the
  * combine kernel's shared memory limit cannot be raised on the current device.  No GPU
@@ -236,7 +236,7 @@ LMOE_API lmoe_status lmoe_debug_inject_wait_timeout(lmoe_ctx* ctx);
 LMOE_API lmoe_status lmoe_debug_check_segments(lmoe_ctx* ctx, lmoe_stream stream);
 
 /* Failure-injection test hook on the host: the next device allocation the library makes for a
- * context workspace (lmoe_create, lmoe_create_fp8) or for lmoe_forward_host's staging buffers
+ * context workspace (lmoe_create, lmoe_create_fp8, lmoe_create_mxfp4) or for lmoe_forward_host's staging buffers
  * fails, and that call returns LMOE_ERR_OOM with nothing leaked.  Process-wide, one shot. */
 LMOE_API void lmoe_debug_fail_next_alloc(void);
 
@@ -248,7 +248,7 @@ LMOE_API void lmoe_debug_fail_next_alloc(void);
  * of kernels those calls launched into *launches (any output may be NULL). */
 #define LMOE_NUM_STAGES 9
 /* stage order: router GEMM, cutoff + top-K + segments, W_down GEMM, routed token rows into slot
- * order (gather; e4m3 quantization too with fp8 experts), expert gate/up GEMM, expert down GEMM,
+ * order (gather; e4m3 quantization too with fp8 or MXFP4 experts), expert gate/up GEMM, expert down GEMM,
  * RMSNorm + combine, shared gate/up GEMM, W_up + shared-down GEMM */
 LMOE_API lmoe_status lmoe_profile(lmoe_ctx* ctx, int32_t enable);
 LMOE_API lmoe_status lmoe_profile_read(lmoe_ctx* ctx, float* ms, int32_t* calls, int64_t* launches);
