@@ -11,7 +11,7 @@ from oracle import lmoe_oracle as O
 from sparse_moe_layer_cutoff_b300 import LatentMoE, LmoeError
 from sparse_moe_layer_cutoff_b300 import lmoe as L
 from sparse_moe_layer_cutoff_b300.lmoe import workspace_tensors
-from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, GAP_MIN, oracle_weights, rel_l2, to64
+from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, GAP_MIN, latent_norm_scale, oracle_weights, rel_l2, to64
 from workloads import WORKLOADS, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -95,12 +95,14 @@ class MxExperts:
         return tuple(out)
 
 
-def _run_mx(wl, bt, rows=None):
+def _run_mx(wl, bt, rows=None, norm="expert"):
     x, weights, bias = make_inputs(wl, "cuda", bt)
     mx = L.quantize_experts_mxfp4(weights)
     s = wl.shape
     dense = {k: v for k, v in weights.items() if not k.startswith("exp_")}
     layer = LatentMoE(s, dense, max_bt=bt, router_bias=bias, mxfp4_experts=mx)
+    if norm != "expert":
+        layer.set_latent_norm(norm)
     r = layer.route(x)
     out = layer.forward(x)
     torch.cuda.synchronize()
@@ -112,11 +114,12 @@ def _run_mx(wl, bt, rows=None):
     # the layer's stored z enters the oracle's per-token e4m3 quantizer (as for the fp8 experts)
     z = to64(workspace_tensors(layer)["z"][torch.as_tensor(rows, device="cuda")])
     want = O.layer_forward_mxfp4(to64(x[rows]), ref["idx"][rows], ref["w"][rows], oracle_weights(weights),
-                                 MxExperts(mx, s), s.beta, s.beta_u, s.rms_eps, z_bf16=z)
+                                 MxExperts(mx, s), s.beta, s.beta_u, s.rms_eps, z_bf16=z, norm=norm)
     got = to64(out[rows])
     m = float(np.abs(got - want).max())
     rl = rel_l2(got, want)
-    assert m <= BF16_MAX_ABS and rl <= BF16_REL_L2, (m, rl)
+    k = latent_norm_scale(z, ref["idx"][rows], ref["w"][rows], oracle_weights(weights), s, norm)
+    assert m <= BF16_MAX_ABS * k and rl <= BF16_REL_L2, (m, rl, k)
     layer.close()
     return m, rl
 
@@ -127,6 +130,13 @@ def test_mxfp4_layer_small_matches_oracle(bt):
     MMA's A side), larger ones with the weights as A (at 2048 tokens experts span several
     192-token tiles)."""
     _run_mx(WORKLOADS["small_bf16"], bt)
+
+
+@pytest.mark.parametrize("bt", [64, 300])
+def test_mxfp4_layer_combined_latent_norm(bt):
+    """The latent norm on the weighted sum with MXFP4 experts (swapped kernels at 64 tokens, weights
+    as A at 300)."""
+    _run_mx(WORKLOADS["small_bf16"], bt, norm="combined")
 
 
 def test_mxfp4_layer_full_decode():
