@@ -229,14 +229,14 @@ def oracle_sample_time(w, x, weights, bias, n_tokens: int, offset: int = 0):
 
 # ----------------------------------------------------------------------------- traffic record
 
-def kernel_traffic(stage: str):
-    """DRAM bytes per launch of `stage` from the committed ncu summary, if the kernel source
-    it was taken from is unchanged (else None)."""
+def kernel_traffic(stage: str, workload: str, experts: str):
+    """DRAM bytes per launch of `stage` from the committed ncu summary, if it was scaled to this
+    workload and expert format and the kernel source it was taken from is unchanged (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     rec = json.load(open(p)).get(stage)
-    if not rec:
+    if not rec or rec.get("workload") != workload or rec.get("experts") != experts:
         return None
     src = os.path.join(ROOT, rec["source"])
     if not os.path.exists(src) or hashlib.sha1(open(src, "rb").read()).hexdigest() != rec["source_sha1"]:
@@ -553,7 +553,7 @@ def main(argv=None):
     else:
         roof = {"bound": "hbm", "achieved": b / (dom_ms / 1e3) / 1e9, "peak": pk["hbm"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = kernel_traffic(dom)
+    roof["traffic"] = kernel_traffic(dom, w.name, "fp8" if args.fp8_experts else "mxfp4" if args.mxfp4_experts else "bf16")
     roof.update({"kernel": dom, "ms_per_launch": dom_ms, "algorithmic_flops": f, "algorithmic_bytes": b,
                  "peak_source": pk["source"] + (" sustained" if (roof["bound"] == "tensor" and long_step) else
                                                 " burst" if roof["bound"] == "tensor" else "")

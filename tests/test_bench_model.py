@@ -84,3 +84,16 @@ def test_layer_fraction_takes_the_binding_roof():
     assert r["tc_frac"] == pytest.approx(11.77e12 / 0.0154 / 1756.5e12, rel=1e-3)
     r = bench.layer_fractions(FULL, 16384, 896, 0.030, pk)
     assert r["bound"] == "tensor" and r["frac"] == r["tc_frac"]
+
+
+def test_traffic_record_applies_only_to_its_workload_and_format():
+    """roofline.traffic comes from the committed ncu record only for the launch it was scaled to
+    (workload and expert format) and only while the kernel source is the one it was taken from."""
+    import json
+    import os
+    rec = json.load(open(os.path.join(os.path.dirname(bench.__file__), "profiles", "traffic.json")))["expert_gate_up_gemm"]
+    got = bench.kernel_traffic("expert_gate_up_gemm", rec["workload"], rec["experts"])
+    assert got in (None, rec["dram_bytes_per_launch"])   # None once the kernel source has changed
+    assert bench.kernel_traffic("expert_gate_up_gemm", "full_decode_bt64", rec["experts"]) is None
+    assert bench.kernel_traffic("expert_gate_up_gemm", rec["workload"], "mxfp4") is None
+    assert bench.kernel_traffic("router_gemm", rec["workload"], rec["experts"]) is None
