@@ -425,36 +425,50 @@ def layer_fractions(shape, bt, n_touched, step_s, pk, fp8_experts=False, mxfp4_e
             "algorithmic_flops": flops, "algorithmic_bytes": layer_bytes, "experts_touched": n_touched}
 
 
-def extra_workload(name, weights, steps, warmup, local, ws, device, pk):
+def extra_workload(name, weights, steps, warmup, local, ws, device, pk, experts="bf16"):
     """One more line of the layer on the bench's weights: the named workload's token batch (its
     own seed, and for the skewed one the Zipf logit bias and the repeated-token block), timed
-    as the headline is.  Returns a dict for the JSON line."""
+    as the headline is; experts "fp8" / "mxfp4" quantize the routed experts first (the
+    quantization is not timed).  Returns a dict for the JSON line."""
     from sparse_moe_layer_cutoff_b300 import LatentMoE
+    from sparse_moe_layer_cutoff_b300.lmoe import quantize_experts_fp8, quantize_experts_mxfp4
     from workloads import make_bias
 
     w = WORKLOADS[name]
     s = w.shape
-    layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=make_bias(w, device))
+    lowp = {}
+    if experts == "fp8":
+        lowp["fp8_experts"] = quantize_experts_fp8(weights)
+    elif experts == "mxfp4":
+        lowp["mxfp4_experts"] = quantize_experts_mxfp4(weights)
+    layer = LatentMoE(s, weights, max_bt=w.bt, router_bias=make_bias(w, device), **lowp)
     xs = [make_x(w, device), make_x(w, device, seed_offset=1)]
     out = torch.empty((w.bt, s.d), dtype=layer.dtype, device=device)
     n_touched, lmax, lmin = routing_stats(layer, xs)
     ms, stage_ms, calls, launches, clk = time_forwards(layer, xs, out, steps, warmup, local, ws)
     layer.close()
-    del xs, out
+    del xs, out, lowp, layer
     torch.cuda.empty_cache()
     step_s = ms / 1e3 / steps
-    fr = layer_fractions(s, w.bt, n_touched, step_s, pk)
-    return {"workload": w.name, "bt": w.bt, "steps": steps, "warmup": warmup, "ms_per_step": ms / steps,
+    fr = layer_fractions(s, w.bt, n_touched, step_s, pk, fp8_experts=experts == "fp8",
+                         mxfp4_experts=experts == "mxfp4")
+    return {"workload": w.name, "experts": experts, "bt": w.bt, "steps": steps, "warmup": warmup,
+            "ms_per_step": ms / steps,
             "tokens_s": w.bt / step_s, "tc_frac": fr["tc_frac"], "hbm_frac": fr["hbm_frac"],
             "bound": fr["bound"], "frac": fr["frac"], "experts_touched": n_touched,
             "expert_load": {"max": lmax, "min": lmin, "target": w.bt * s.top_k / s.n_experts},
             "stage_ms_per_step": {k: v / max(calls, 1) for k, v in stage_ms.items()},
             "gpu_launches": launches, "clocks": clk,
-            "inputs": "the headline's weights; x drawn with this workload's seed" +
+            "inputs": "the headline's weights" +
+                      ("" if experts == "bf16" else f" (routed experts quantized to {experts}, not timed)") +
+                      "; x drawn with this workload's seed" +
                       (", Zipf(1.1) logit bias and 25 % identical tokens" if w.zipf_bias else "")}
 
 
-EXTRA_WORKLOADS = ("full_decode_bt64", "full_skewed_bt16384")
+# extra figures of the default line: (JSON key, workload, routed-expert format)
+EXTRA_WORKLOADS = (("decode_bt64", "full_decode_bt64", "bf16"), ("skewed_bt16384", "full_skewed_bt16384", "bf16"),
+                   ("decode_bt64_fp8_experts", "full_decode_bt64", "fp8"),
+                   ("decode_bt64_mxfp4_experts", "full_decode_bt64", "mxfp4"))
 
 
 def main(argv=None):
@@ -602,8 +616,8 @@ def main(argv=None):
         layer.close()
         del xs, out, xh, oh
         torch.cuda.empty_cache()
-        for name in EXTRA_WORKLOADS:
-            extras[name] = extra_workload(name, weights, args.steps, args.warmup, local, ws, device, pk)
+        for key, name, experts in EXTRA_WORKLOADS:
+            extras[key] = extra_workload(name, weights, args.steps, args.warmup, local, ws, device, pk, experts)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
@@ -631,9 +645,7 @@ def main(argv=None):
         if args.latent_norm != "expert":
             line["metric"] += f" [latent norm: {args.latent_norm}]"
             line["config"]["latent_norm"] = args.latent_norm
-        if extras:
-            line["decode_bt64"] = extras["full_decode_bt64"]
-            line["skewed_bt16384"] = extras["full_skewed_bt16384"]
+        line.update(extras)
         print(json.dumps(line), flush=True)
     if not default_line:
         layer.close()
