@@ -101,6 +101,7 @@ def _run_fp8(wl, bt, rows=None, norm="expert"):
                              s.beta_u, s.rms_eps, norm=norm)
     assert rel_l2(got, want16) < 0.1
     layer.close()
+    return out
 
 
 @pytest.mark.parametrize("bt", [300, 1, 77, 2048])
@@ -139,3 +140,12 @@ def test_create_fp8_argument_errors():
     with pytest.raises(LmoeError):
         LatentMoE(WORKLOADS["tiny_f32"].shape, make_inputs(WORKLOADS["tiny_f32"], "cuda", 8)[1], max_bt=8,
                   fp8_experts=f8)
+
+
+def test_fp8_layer_skewed_routing_small():
+    """Zipf logit bias and 25 % identical tokens on the small shape at 2048 tokens: the identical
+    tokens' experts run several token tiles; identical tokens give identical outputs, bit for bit."""
+    w = WORKLOADS["small_bf16"].with_(zipf_bias=True, repeat_frac=0.25, seed=4)
+    out = _run_fp8(w, w.bt)
+    nrep = int(round(w.bt * 0.25))
+    assert torch.equal(out[:nrep], out[:1].expand(nrep, -1))

@@ -121,7 +121,7 @@ def _run_mx(wl, bt, rows=None, norm="expert"):
     k = latent_norm_scale(z, ref["idx"][rows], ref["w"][rows], oracle_weights(weights), s, norm)
     assert m <= BF16_MAX_ABS * k and rl <= BF16_REL_L2, (m, rl, k)
     layer.close()
-    return m, rl
+    return out
 
 
 @pytest.mark.parametrize("bt", [300, 1, 77, 128, 129, 2048])
@@ -163,3 +163,12 @@ def test_create_mxfp4_argument_errors():
     with pytest.raises(LmoeError):
         LatentMoE(WORKLOADS["tiny_f32"].shape, make_inputs(WORKLOADS["tiny_f32"], "cuda", 8)[1], max_bt=8,
                   mxfp4_experts=mx)
+
+
+def test_mxfp4_layer_skewed_routing_small():
+    """Zipf logit bias and 25 % identical tokens on the small shape at 2048 tokens: the identical
+    tokens' experts run several token tiles; identical tokens give identical outputs, bit for bit."""
+    w = WORKLOADS["small_bf16"].with_(zipf_bias=True, repeat_frac=0.25, seed=4)
+    out = _run_mx(w, w.bt)
+    nrep = int(round(w.bt * 0.25))
+    assert torch.equal(out[:nrep], out[:1].expand(nrep, -1))
