@@ -236,3 +236,16 @@ def test_mxfp4_block_scales_tiled_instead_of_repeated_is_caught(monkeypatch):
                         np.tile(np.exp2(np.asarray(x, np.float64)), 32))
     assert _fails(P.test_dequantize_mxfp4_per_element)
     assert _fails(P.test_mxfp4_routed_latent_matches_brute_force)
+
+
+def test_lowp_layer_without_shared_experts_is_caught(monkeypatch):
+    monkeypatch.setattr(O, "shared_experts", lambda x, weights, beta, beta_u: np.zeros((np.asarray(x).shape[0],
+                                                                                     np.asarray(weights["w_up"]).shape[0])))
+    assert _fails(lambda: P.test_lowp_layer_is_up_projection_of_routed_latent_plus_shared("fp8"))
+    assert _fails(lambda: P.test_lowp_layer_is_up_projection_of_routed_latent_plus_shared("mxfp4"))
+
+
+def test_lowp_layer_with_unrounded_z_is_caught(monkeypatch):
+    # z = x W_down^T left in fp64 instead of rounded to bf16 as the layer stores it
+    monkeypatch.setattr(O, "bf16_round", lambda v: np.asarray(v, np.float64))
+    assert _fails(lambda: P.test_lowp_layer_is_up_projection_of_routed_latent_plus_shared("fp8"))

@@ -867,3 +867,48 @@ def test_mxfp4_routed_latent_is_close_to_bf16_one():
     rel = np.linalg.norm(got - ref) / np.linalg.norm(ref)
     rel8 = np.linalg.norm(got8 - ref) / np.linalg.norm(ref)
     assert rel8 < rel < 0.3, (rel, rel8)
+
+
+# ----------------------------------------------------------------- low-precision layer composition
+
+def _torch_shared(x, sg, su, sd, beta, beta_u):
+    """Shared experts by torch ops: sum_j W_d^j act(W_g^j x, W_u^j x), act = g' sigmoid(g') u'."""
+    xt = torch.from_numpy(x)
+    out = torch.zeros(x.shape[0], sd.shape[1], dtype=torch.float64)
+    for j in range(sg.shape[0]):
+        g = F.linear(xt, torch.from_numpy(sg[j]))
+        u = F.linear(xt, torch.from_numpy(su[j]))
+        gp = beta * torch.tanh(g / beta)
+        up = beta_u * torch.tanh(u / beta_u)
+        out += F.linear(gp * torch.sigmoid(gp) * up, torch.from_numpy(sd[j]))
+    return out.numpy()
+
+
+@pytest.mark.parametrize("fmt", ["fp8", "mxfp4"])
+def test_lowp_layer_is_up_projection_of_routed_latent_plus_shared(fmt):
+    """layer_forward_fp8 / layer_forward_mxfp4: z is x W_down^T rounded to bf16 (torch's conversion)
+    unless given, the output is W_up (routed latent of z) plus the shared experts (computed here
+    with torch ops), for both latent-norm placements."""
+    rng = np.random.default_rng(41)
+    bt, d, L, E, K, I, S, Is = 5, 64, 32, 4, 2, 32, 2, 64
+    x = rng.normal(size=(bt, d))
+    W = {"w_down": rng.normal(size=(L, d)) / 8, "w_up": rng.normal(size=(d, L)) / 6,
+         "latent_gamma": 1 + 0.1 * rng.normal(size=L),
+         "sh_gate": rng.normal(size=(S, Is, d)) / 8, "sh_up": rng.normal(size=(S, Is, d)) / 8,
+         "sh_down": rng.normal(size=(S, d, Is)) / 8}
+    q = O.quantize_rows_e4m3 if fmt == "fp8" else O.quantize_rows_mxfp4
+    wq = {e: (q(rng.normal(size=(I, L)) / 5), q(rng.normal(size=(I, L)) / 5), q(rng.normal(size=(L, I)) / 5))
+          for e in range(E)}
+    idx = np.array([[0, 1], [2, 3], [1, 0], [3, 2], [0, 2]], np.int32)
+    w = np.array([[0.6, 0.4], [0.5, 0.5], [0.7, 0.3], [0.2, 0.8], [0.9, 0.1]])
+    z = torch.from_numpy(x @ W["w_down"].T).to(torch.float32).to(torch.bfloat16).to(torch.float64).numpy()
+    shared = _torch_shared(x, W["sh_gate"], W["sh_up"], W["sh_down"], 4.0, 25.0)
+    fwd = O.layer_forward_fp8 if fmt == "fp8" else O.layer_forward_mxfp4
+    routed = O.routed_latent_fp8 if fmt == "fp8" else O.routed_latent_mxfp4
+    for norm in ("expert", "combined"):
+        want = routed(z, idx, w, wq, W["latent_gamma"], 4.0, 25.0, 1e-6, norm) @ W["w_up"].T + shared
+        np.testing.assert_allclose(fwd(x, idx, w, W, wq, norm=norm), want, rtol=1e-12, atol=1e-12)
+        # a given stored z is used as is
+        z2 = z + 0.25
+        want2 = routed(z2, idx, w, wq, W["latent_gamma"], 4.0, 25.0, 1e-6, norm) @ W["w_up"].T + shared
+        np.testing.assert_allclose(fwd(x, idx, w, W, wq, z_bf16=z2, norm=norm), want2, rtol=1e-12, atol=1e-12)
