@@ -491,7 +491,7 @@ def main(argv=None):
     ap.add_argument("--latent-norm", default="expert", choices=["expert", "combined"],
                     help="latent RMSNorm placement; 'combined' (one norm of the weighted sum) is a separate line")
     ap.add_argument("--no-extra", action="store_true",
-                    help="skip the decode (64 tokens) and skewed (16384 tokens) figures of the default line")
+                    help="skip the extra figures of the default line (64-token decode with bf16, e4m3 and MXFP4 experts; 16384-token skewed forward)")
     args = ap.parse_args(argv)
     if args.e2e_steps is None:
         args.e2e_steps = args.steps
