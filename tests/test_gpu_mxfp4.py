@@ -12,7 +12,7 @@ from sparse_moe_layer_cutoff_b300 import LatentMoE, LmoeError
 from sparse_moe_layer_cutoff_b300 import lmoe as L
 from sparse_moe_layer_cutoff_b300.lmoe import workspace_tensors
 from tests.lmoe_testing import BF16_MAX_ABS, BF16_REL_L2, GAP_MIN, latent_norm_scale, oracle_weights, rel_l2, to64
-from workloads import WORKLOADS, make_inputs
+from workloads import WORKLOADS, make_inputs, make_x
 
 pytestmark = pytest.mark.gpu
 
@@ -172,3 +172,36 @@ def test_mxfp4_layer_skewed_routing_small():
     out = _run_mx(w, w.bt)
     nrep = int(round(w.bt * 0.25))
     assert torch.equal(out[:nrep], out[:1].expand(nrep, -1))
+
+
+@pytest.mark.parametrize("bt", [64, 300])
+def test_mxfp4_forward_replays_in_a_cuda_graph(bt):
+    """The MXFP4 layer (swapped kernels at 64 tokens, weights as A at 300) captured in a CUDA graph:
+    replays with new contents in the captured input buffer give the same bits as eager calls."""
+    wl = WORKLOADS["small_bf16"]
+    x0, weights, bias = make_inputs(wl, "cuda", bt)
+    x1 = make_x(wl, "cuda", bt, seed_offset=9)
+    mx = L.quantize_experts_mxfp4(weights)
+    dense = {k: v for k, v in weights.items() if not k.startswith("exp_")}
+    layer = LatentMoE(wl.shape, dense, max_bt=bt, router_bias=bias, mxfp4_experts=mx)
+    eager0 = layer.forward(x0)
+    eager1 = layer.forward(x1)
+    torch.cuda.synchronize()
+    xin = x0.clone()
+    out = torch.empty_like(eager0)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(xin, out, stream=s)      # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        layer.forward(xin, out, stream=s)
+    for xb, want in ((x1, eager1), (x0, eager0), (x1, eager1)):
+        xin.copy_(xb)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, want)
+    assert layer.sync_status() == 0
+    layer.close()
