@@ -258,9 +258,9 @@ def test_full_skewed_bt16384():
     slots = []
     for e in heavy:
         lo, hi = int(off[e]), int(off[e + 1])
-        tile = 192                   # token tile of the grouped GEMMs
+        tile = 256                   # token tile of the bf16 routed-expert GEMMs
         for b in range(lo, hi, tile):
-            slots += [b, min(b + tile, hi) - 1]
+            slots += [b, min(b + 1, hi - 1), min(b + tile, hi) - 1]
         slots += rng.integers(lo, hi, size=4).tolist()
     n, ne = _check_expert_slots(r, ref, slots)
     assert n >= 64 and ne == len(heavy)
